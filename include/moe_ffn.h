@@ -1,0 +1,174 @@
+/*
+ * moe_ffn.h — C ABI of the Gemma-4 26B-A4B sparse MoE feed-forward block on one GB300 (sm_103a).
+ *
+ * What the block computes is defined by the blog post "Porting a 128-expert MoE (Gemma-4 26B-A4B)
+ * to AWS Inferentia2 — where every rank weighted the wrong experts", section "The architecture: a
+ * dual-path FFN nobody warned me about": from the post-attention residual x, a dense branch
+ * (pre_feedforward_layernorm -> shared MLP of width 2112 -> post_feedforward_layernorm_1) and an
+ * expert branch (pre_feedforward_layernorm_2 -> router -> 128 experts of width 704 ->
+ * post_feedforward_layernorm_2) are added, normalised by post_feedforward_layernorm, added to the
+ * residual and multiplied by layer_scalar. The router has its own RMSNorm, a scale and a
+ * per-expert scale; it takes an fp32 softmax over the 128 experts, keeps the top 8, renormalises
+ * them to sum 1 and multiplies by per_expert_scale. The experts hold a fused gate_up projection
+ * [128,1408,2816] and a down projection [128,2816,704]. The activation is the tanh form of GELU
+ * ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", §4.5; "Lab 008 — Raw lab detail",
+ * "The model under test": hidden_activation=gelu_pytorch_tanh). layer_scalar is a per-layer
+ * buffer that weight loaders that copy parameters only silently drop (same page, §4.6), so here it
+ * is a required field of the weights with no default.
+ *
+ * Conventions for every entry point:
+ *   - Return value: an int status (MOE_FFN_OK or a negative MOE_FFN_E* code). No entry point
+ *     aborts, throws or prints; moe_ffn_status_string() names a code.
+ *   - "device pointer" means memory of the CUDA device the context was created on; "host pointer"
+ *     means ordinary process memory. Every pointer is borrowed: the library never frees memory it
+ *     did not allocate, and the caller keeps each buffer alive while work that uses it is queued.
+ *   - A stream argument is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     moe_ffn_forward only enqueues work on that stream: it does not synchronise the host, does
+ *     not allocate device memory and does not read anything back to the host.
+ *   - Tensors are dense and row-major (last index fastest); bf16 is IEEE bfloat16 stored as 16-bit
+ *     words. Every device pointer must be 16-byte aligned (MOE_FFN_EALIGN otherwise).
+ *   - There is no CPU fallback: without an sm_103 device the calls fail with MOE_FFN_EARCH or
+ *     MOE_FFN_ECUDA.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define MOE_FFN_OK 0
+#define MOE_FFN_EINVAL (-1)   /* a NULL pointer, a size out of range or a dimension other than the model's */
+#define MOE_FFN_EALIGN (-2)   /* a device pointer not 16-byte aligned */
+#define MOE_FFN_ETOOBIG (-3)  /* T above the context's max_tokens, or a workspace smaller than required */
+#define MOE_FFN_EARCH (-4)    /* the device is not compute capability 10.3 (sm_103) */
+#define MOE_FFN_ECUDA (-5)    /* a CUDA runtime or driver call failed */
+#define MOE_FFN_EDEVICE (-6)  /* a kernel gave up a bounded wait or found a bad index and set the status word */
+
+/* Modes. */
+#define MOE_FFN_MOE_ONLY 0    /* router + experts only: out = sum of the 8 weighted expert outputs */
+#define MOE_FFN_FULL_LAYER 1  /* the whole dual-path feed-forward layer with norms, residual, layer_scalar */
+
+/* Model dimensions of Gemma-4 26B-A4B ("Lab 008 — Raw lab detail", "The model under test";
+ * top-8 and the gate_up/down shapes from the 26B-A4B post, "The architecture"). The kernels are
+ * built for exactly these; moe_ffn_init rejects any other value with MOE_FFN_EINVAL. */
+#define MOE_FFN_HIDDEN 2816
+#define MOE_FFN_N_EXPERTS 128
+#define MOE_FFN_TOP_K 8
+#define MOE_FFN_MOE_INTER 704
+#define MOE_FFN_DENSE_INTER 2112
+#define MOE_FFN_MAX_TOKENS_LIMIT 65536
+
+typedef struct moe_ffn_config {
+  int hidden;          /* must be 2816 */
+  int n_experts;       /* must be 128 */
+  int top_k;           /* must be 8 */
+  int moe_inter;       /* must be 704 */
+  int dense_inter;     /* must be 2112 */
+  int mode;            /* MOE_FFN_MOE_ONLY or MOE_FFN_FULL_LAYER */
+  int max_tokens;      /* the largest T a forward call on this context may pass, 1..65536 */
+  float eps;           /* RMSNorm epsilon for all six norms, > 0 (1e-6 for this model) */
+  float router_scale;  /* scalar applied to the router's normed input, > 0 (2816^-1/2) */
+} moe_ffn_config;
+
+/* Weights of one layer. Every pointer is a DEVICE pointer, borrowed. RMSNorm weights are in the
+ * Gemma form: a norm multiplies by (1 + w). In MOE_FFN_MOE_ONLY mode the dense and norm fields
+ * other than router_norm_w are ignored and may be NULL; layer_scalar is still read and ignored. */
+typedef struct moe_ffn_weights {
+  const float* router_w;          /* [128, 2816] fp32: router projection, row e gives expert e's logit */
+  const float* router_norm_w;     /* [2816] fp32: the router's own RMSNorm weight */
+  const float* per_expert_scale;  /* [128] fp32 */
+  const uint16_t* gate_up;        /* [128, 1408, 2816] bf16: rows 0..703 gate, rows 704..1407 up */
+  const uint16_t* down;           /* [128, 2816, 704] bf16 */
+  const uint16_t* dense_gate;     /* [2112, 2816] bf16 (FULL_LAYER) */
+  const uint16_t* dense_up;       /* [2112, 2816] bf16 (FULL_LAYER) */
+  const uint16_t* dense_down;     /* [2816, 2112] bf16 (FULL_LAYER) */
+  const float* pre_ff_ln;         /* [2816] fp32: pre_feedforward_layernorm (dense branch input) */
+  const float* pre_ff_ln_2;       /* [2816] fp32: pre_feedforward_layernorm_2 (expert branch input) */
+  const float* post_ff_ln_1;      /* [2816] fp32: post_feedforward_layernorm_1 (dense branch output) */
+  const float* post_ff_ln_2;      /* [2816] fp32: post_feedforward_layernorm_2 (expert branch output) */
+  const float* post_ff_ln;        /* [2816] fp32: post_feedforward_layernorm (after the sum) */
+  float layer_scalar;             /* required; multiplies (residual + normed sum) */
+} moe_ffn_weights;
+
+/* Device views into the workspace, filled by moe_ffn_workspace_view. Contents are those of the
+ * last forward queued on the context and are valid once that forward has completed, until the
+ * next forward. S = 8*T slots; slot (t, k) is token t's k-th selected expert, k ascending in
+ * expert id. */
+typedef struct moe_ffn_views {
+  const float* logits;        /* [T, 128] fp32 router logits */
+  const int32_t* topk_idx;    /* [T, 8] selected experts, ascending expert id */
+  const float* topk_w;        /* [T, 8] renormalised weights times per_expert_scale, same order */
+  const float* gap;           /* [T] 8th-largest minus 9th-largest logit */
+  const int32_t* counts;      /* [128] slots per expert */
+  const int32_t* offsets;     /* [129] exclusive prefix sum of counts; offsets[128] = S */
+  const int32_t* perm;        /* [S] token of each slot in expert-major, token-ascending order */
+  const float* w_sorted;      /* [S] the weight of each sorted slot */
+  const int32_t* slot_pos;    /* [T, 8] sorted position of slot (t, k) */
+  const uint16_t* n1;         /* [T, 2816] bf16 pre_feedforward_layernorm(x) (FULL_LAYER) */
+  const uint16_t* n2;         /* [T, 2816] bf16 expert input: pre_feedforward_layernorm_2(x), or x */
+  const uint16_t* h;          /* [S, 704] bf16 gelu_tanh(gate) * up per sorted slot */
+  const uint16_t* h_dense;    /* [T, 2112] bf16 shared-MLP activation (FULL_LAYER) */
+  const float* y;             /* [S, 2816] fp32 weighted expert output per sorted slot */
+  const float* d;             /* [T, 2816] fp32 shared-MLP output (FULL_LAYER) */
+  int T;                      /* tokens of that forward */
+} moe_ffn_views;
+
+typedef struct moe_ffn_ctx moe_ffn_ctx;
+
+/* Bytes of device workspace a context with this config needs (0 if the config is invalid). */
+size_t moe_ffn_workspace_bytes(const moe_ffn_config* cfg);
+
+/* Creates a context on CUDA device `device` (which this call makes current). `workspace` is a
+ * device pointer to at least moe_ffn_workspace_bytes(cfg) bytes, 256-byte aligned, that the
+ * context uses for its intermediates; the caller owns it. Several contexts may share one workspace
+ * if their forwards never overlap in time (e.g. all on one stream). Fails with MOE_FFN_EARCH on a
+ * device other than sm_103. On failure *ctx is set to NULL. */
+int moe_ffn_init(moe_ffn_ctx** ctx, const moe_ffn_config* cfg, void* workspace,
+                 size_t workspace_bytes, int device);
+
+/* Queues one forward of the block on `stream`: out = block(x) for T tokens.
+ *   x   device pointer, [T, 2816] bf16, the layer input (the post-attention residual).
+ *   T   0..max_tokens; T = 0 queues nothing and returns MOE_FFN_OK.
+ *   w   host pointer to a weights struct whose fields are device pointers; the struct is read
+ *       during the call, the tensors it names are read by the queued kernels.
+ *   out device pointer, [T, 2816] bf16; must not overlap x or the workspace.
+ * The result is deterministic: the same inputs give bitwise-equal outputs. Errors found while
+ * queueing are returned; errors found by the kernels set the device status word (see
+ * moe_ffn_device_status). */
+int moe_ffn_forward(moe_ffn_ctx* ctx, const void* x, int T, const moe_ffn_weights* w, void* out,
+                    void* stream);
+
+/* Fills *views with device pointers into the workspace (see moe_ffn_views). */
+int moe_ffn_workspace_view(const moe_ffn_ctx* ctx, moe_ffn_views* views);
+
+/* Synchronises `stream`, reads the device status word and clears it. Returns MOE_FFN_EDEVICE if a
+ * kernel gave up a bounded wait or rejected an index since the last call, MOE_FFN_ECUDA if the
+ * stream reported a CUDA error, else MOE_FFN_OK. *word (if not NULL) receives the raw status bits. */
+int moe_ffn_device_status(moe_ffn_ctx* ctx, void* stream, uint32_t* word);
+
+/* Profiling hook: from now on every forward records `start` (a cudaEvent_t as void*) on its stream
+ * right before the launch of kernel `kernel` and `stop` right after it. NULL events turn the hook
+ * off. kernel: 0 router logits, 1 top-k and pre-norms, 2 permutation, 3 gate_up grouped GEMM,
+ * 4 down grouped GEMM, 5 combine and post-norms. */
+int moe_ffn_set_kernel_events(moe_ffn_ctx* ctx, int kernel, void* start, void* stop);
+
+/* Number of kernels one forward of T tokens launches on the device (0 for T = 0). */
+int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
+
+/* A static string naming a status code. */
+const char* moe_ffn_status_string(int status);
+
+/* Releases the host state of a context (it holds no device memory). Never frees the workspace or
+ * any caller buffer. Safe on NULL. */
+void moe_ffn_destroy(moe_ffn_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

@@ -1,0 +1,323 @@
+/*
+ * moe_oracle.c — the oracle (test infrastructure only; see moe_oracle.h for sources and
+ * precision). Plain loops, one token at a time, in the order the pages describe the block:
+ *
+ *   residual x
+ *   ├─ dense:  pre_feedforward_layernorm   → shared MLP (D)        → post_feedforward_layernorm_1
+ *   └─ expert: pre_feedforward_layernorm_2 → router → K of E experts → post_feedforward_layernorm_2
+ *   hidden = dense + expert → post_feedforward_layernorm → + residual → × layer_scalar
+ *
+ * ([MoE] "The architecture: a dual-path FFN nobody warned me about"; [Port] §4.6 for layer_scalar.)
+ * Built with -ffp-contract=off so that no multiply-add is fused and x86 and Arm hosts give the
+ * same bits.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 is the upper half of an IEEE fp32 word, so widening is exact. */
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* [Port] §4.5: 0.5*x*(1+tanh(0.7978845608*(x + 0.044715*x^3))). */
+double moe_oracle_gelu_tanh(double x) {
+  return 0.5 * x * (1.0 + tanh(0.7978845608 * (x + 0.044715 * x * x * x)));
+}
+
+/* Gemma RMSNorm (x / rms(x) * (1 + w)), fp64. */
+void moe_oracle_rmsnorm(const double* v, const float* w, int n, double eps, double* out) {
+  double ss = 0.0;
+  for (int i = 0; i < n; ++i) ss += v[i] * v[i];
+  double inv = 1.0 / sqrt(ss / (double)n + eps);
+  for (int i = 0; i < n; ++i) out[i] = v[i] * inv * (1.0 + (double)w[i]);
+}
+
+/* The router of one token, fp32 ([MoE] "The architecture": its own RMSNorm + a scale, then
+ * softmax over the experts in fp32 → top-K → renormalise → × per_expert_scale).
+ * xin: the router's input vector [H] in fp32. Writes logits[E], probs[E], the K selected experts
+ * in ascending id with their renormalised and scaled weights, and the K-th/(K+1)-th logit gap. */
+static void route_one(const moe_oracle_dims* d, const float* xin, const moe_oracle_weights* w,
+                      float* r, float* logits, float* probs, int32_t* idx, float* wren,
+                      float* wfin, float* gap) {
+  const int H = d->hidden, E = d->n_experts, K = d->top_k;
+
+  /* RMSNorm of the router input, then the scalar scale. */
+  float ss = 0.0f;
+  for (int h = 0; h < H; ++h) ss += xin[h] * xin[h];
+  float inv = 1.0f / sqrtf(ss / (float)H + d->eps);
+  for (int h = 0; h < H; ++h) r[h] = xin[h] * inv * (1.0f + w->router_norm_w[h]) * d->router_scale;
+
+  /* Projection to one logit per expert. */
+  for (int e = 0; e < E; ++e) {
+    const float* row = w->router_w + (size_t)e * H;
+    float acc = 0.0f;
+    for (int h = 0; h < H; ++h) acc += r[h] * row[h];
+    logits[e] = acc;
+  }
+
+  /* Softmax with the maximum subtracted. */
+  float m = logits[0];
+  for (int e = 1; e < E; ++e)
+    if (logits[e] > m) m = logits[e];
+  float z = 0.0f;
+  for (int e = 0; e < E; ++e) {
+    probs[e] = expf(logits[e] - m);
+    z += probs[e];
+  }
+  for (int e = 0; e < E; ++e) probs[e] = probs[e] / z;
+
+  /* Top-K by logit (softmax is monotone in the logit), larger first, lower id first on equal
+   * logits: K+1 rounds of arg-max over the experts not yet taken. */
+  int taken[1024];
+  int order[1025];
+  for (int e = 0; e < E; ++e) taken[e] = 0;
+  int rounds = (K < E) ? K + 1 : K;
+  for (int j = 0; j < rounds; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || logits[e] > logits[best]) best = e; /* '>' keeps the lower id on ties */
+    }
+    taken[best] = 1;
+    order[j] = best;
+  }
+  *gap = (K < E) ? logits[order[K - 1]] - logits[order[K]] : 0.0f;
+
+  /* The selected set, listed in ascending expert id. */
+  int n = 0;
+  for (int e = 0; e < E; ++e) {
+    int sel = 0;
+    for (int j = 0; j < K; ++j)
+      if (order[j] == e) sel = 1;
+    if (sel) idx[n++] = e;
+  }
+
+  /* Renormalise the selected probabilities to sum 1, then multiply by per_expert_scale. */
+  float s = 0.0f;
+  for (int j = 0; j < K; ++j) s += probs[idx[j]];
+  for (int j = 0; j < K; ++j) {
+    wren[j] = probs[idx[j]] / s;
+    wfin[j] = wren[j] * w->per_expert_scale[idx[j]];
+  }
+}
+
+/* One expert's MLP on input v[H] ([MoE] "The architecture": fused gate_up [E,2I,H], down [E,H,I];
+ * [Lab] gelu_pytorch_tanh): hvec = gelu_tanh(gate·v) * (up·v), y = down·hvec. */
+static void expert_mlp(const moe_oracle_dims* d, const moe_oracle_weights* w, int e,
+                       const double* v, double* hvec, double* y) {
+  const int H = d->hidden, I = d->moe_inter;
+  const uint16_t* gate = w->gate_up + (size_t)e * 2 * I * H;
+  const uint16_t* up = gate + (size_t)I * H;
+  for (int i = 0; i < I; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int h = 0; h < H; ++h) {
+      g += (double)bf16_to_f32(gate[(size_t)i * H + h]) * v[h];
+      u += (double)bf16_to_f32(up[(size_t)i * H + h]) * v[h];
+    }
+    hvec[i] = moe_oracle_gelu_tanh(g) * u;
+  }
+  const uint16_t* down = w->down + (size_t)e * H * I;
+  for (int h = 0; h < H; ++h) {
+    double acc = 0.0;
+    for (int i = 0; i < I; ++i) acc += (double)bf16_to_f32(down[(size_t)h * I + i]) * hvec[i];
+    y[h] = acc;
+  }
+}
+
+/* The shared dense MLP ([MoE] "The architecture": mlp (2112)), same gating as the experts. */
+static void dense_mlp(const moe_oracle_dims* d, const moe_oracle_weights* w, const double* v,
+                      double* hvec, double* y) {
+  const int H = d->hidden, D = d->dense_inter;
+  for (int i = 0; i < D; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int h = 0; h < H; ++h) {
+      g += (double)bf16_to_f32(w->dense_gate[(size_t)i * H + h]) * v[h];
+      u += (double)bf16_to_f32(w->dense_up[(size_t)i * H + h]) * v[h];
+    }
+    hvec[i] = moe_oracle_gelu_tanh(g) * u;
+  }
+  for (int h = 0; h < H; ++h) {
+    double acc = 0.0;
+    for (int i = 0; i < D; ++i) acc += (double)bf16_to_f32(w->dense_down[(size_t)h * D + i]) * hvec[i];
+    y[h] = acc;
+  }
+}
+
+static int dims_ok(const moe_oracle_dims* d) {
+  if (!d) return 0;
+  if (d->hidden < 1 || d->n_experts < 1 || d->n_experts > 1024) return 0;
+  if (d->top_k < 1 || d->top_k > d->n_experts) return 0;
+  if (d->moe_inter < 1) return 0;
+  if (d->full_layer && d->dense_inter < 1) return 0;
+  if (!(d->eps > 0.0f)) return 0;
+  return 1;
+}
+
+int moe_oracle_forward(const moe_oracle_dims* d, int T, const uint16_t* x,
+                       const moe_oracle_weights* w, const moe_oracle_outputs* o, int masked_dense) {
+  if (!dims_ok(d) || T < 0 || !w || !o || (T > 0 && !x)) return -1;
+  const int H = d->hidden, E = d->n_experts, K = d->top_k, I = d->moe_inter;
+  const int D = d->full_layer ? d->dense_inter : 1;
+  int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int t = 0; t < T; ++t) {
+    double* xd = malloc(sizeof(double) * H);
+    double* n1 = malloc(sizeof(double) * H);
+    double* n2 = malloc(sizeof(double) * H);
+    double* moe = malloc(sizeof(double) * H);
+    double* y = malloc(sizeof(double) * H);
+    double* dn = malloc(sizeof(double) * H);
+    double* hv = malloc(sizeof(double) * (I > D ? I : D));
+    float* xin = malloc(sizeof(float) * H);
+    float* r = malloc(sizeof(float) * H);
+    float* logits = malloc(sizeof(float) * E);
+    float* probs = malloc(sizeof(float) * E);
+    int32_t* idx = malloc(sizeof(int32_t) * K);
+    float* wren = malloc(sizeof(float) * K);
+    float* wfin = malloc(sizeof(float) * K);
+    if (!xd || !n1 || !n2 || !moe || !y || !dn || !hv || !xin || !r || !logits || !probs || !idx ||
+        !wren || !wfin) {
+      bad |= 1;
+    } else {
+      for (int h = 0; h < H; ++h) xd[h] = (double)bf16_to_f32(x[(size_t)t * H + h]);
+
+      /* Branch inputs: the two pre-norms in the full layer; raw x for the experts otherwise. */
+      if (d->full_layer) {
+        moe_oracle_rmsnorm(xd, w->pre_ff_ln, H, (double)d->eps, n1);
+        moe_oracle_rmsnorm(xd, w->pre_ff_ln_2, H, (double)d->eps, n2);
+      } else {
+        for (int h = 0; h < H; ++h) n2[h] = xd[h];
+      }
+
+      /* Router input: the layer input x, or (alternative reading) pre_feedforward_layernorm_2(x). */
+      for (int h = 0; h < H; ++h)
+        xin[h] = (d->full_layer && d->router_reads_pre2) ? (float)n2[h] : (float)xd[h];
+      float gap;
+      route_one(d, xin, w, r, logits, probs, idx, wren, wfin, &gap);
+
+      /* Expert branch: sum over experts in ascending id, starting from +0. */
+      for (int h = 0; h < H; ++h) moe[h] = 0.0;
+      if (!masked_dense) {
+        for (int k = 0; k < K; ++k) {
+          expert_mlp(d, w, idx[k], n2, hv, y);
+          if (o->h_slot)
+            for (int i = 0; i < I; ++i) o->h_slot[((size_t)t * K + k) * I + i] = hv[i];
+          for (int h = 0; h < H; ++h) {
+            double c = (double)wfin[k] * y[h];
+            moe[h] += c;
+            if (o->y_slot) o->y_slot[((size_t)t * K + k) * H + h] = c;
+          }
+        }
+      } else {
+        /* Every expert, weighted by its router weight or by 0 when it is not selected: a
+         * non-selected expert adds 0 * y = ±0, which leaves the running sum unchanged. */
+        int k = 0;
+        for (int e = 0; e < E; ++e) {
+          double we = 0.0;
+          int is_sel = (k < K && idx[k] == e);
+          if (is_sel) we = (double)wfin[k];
+          expert_mlp(d, w, e, n2, hv, y);
+          if (is_sel && o->h_slot)
+            for (int i = 0; i < I; ++i) o->h_slot[((size_t)t * K + k) * I + i] = hv[i];
+          for (int h = 0; h < H; ++h) {
+            double c = we * y[h];
+            moe[h] += c;
+            if (is_sel && o->y_slot) o->y_slot[((size_t)t * K + k) * H + h] = c;
+          }
+          if (is_sel) ++k;
+        }
+      }
+
+      if (d->full_layer) {
+        dense_mlp(d, w, n1, hv, dn);
+        if (o->h_dense)
+          for (int i = 0; i < D; ++i) o->h_dense[(size_t)t * D + i] = hv[i];
+        if (o->dense)
+          for (int h = 0; h < H; ++h) o->dense[(size_t)t * H + h] = dn[h];
+        if (o->moe)
+          for (int h = 0; h < H; ++h) o->moe[(size_t)t * H + h] = moe[h];
+        /* post_feedforward_layernorm_1 on the dense branch, _2 on the expert branch, add, then
+         * post_feedforward_layernorm, + residual, × layer_scalar. */
+        moe_oracle_rmsnorm(dn, w->post_ff_ln_1, H, (double)d->eps, dn);
+        moe_oracle_rmsnorm(moe, w->post_ff_ln_2, H, (double)d->eps, moe);
+        for (int h = 0; h < H; ++h) y[h] = dn[h] + moe[h];
+        moe_oracle_rmsnorm(y, w->post_ff_ln, H, (double)d->eps, y);
+        if (o->out)
+          for (int h = 0; h < H; ++h)
+            o->out[(size_t)t * H + h] = (xd[h] + y[h]) * (double)w->layer_scalar;
+      } else {
+        if (o->moe)
+          for (int h = 0; h < H; ++h) o->moe[(size_t)t * H + h] = moe[h];
+        if (o->out)
+          for (int h = 0; h < H; ++h) o->out[(size_t)t * H + h] = moe[h];
+      }
+
+      if (o->logits) memcpy(o->logits + (size_t)t * E, logits, sizeof(float) * E);
+      if (o->probs) memcpy(o->probs + (size_t)t * E, probs, sizeof(float) * E);
+      if (o->topk_idx) memcpy(o->topk_idx + (size_t)t * K, idx, sizeof(int32_t) * K);
+      if (o->topk_w_renorm) memcpy(o->topk_w_renorm + (size_t)t * K, wren, sizeof(float) * K);
+      if (o->topk_w) memcpy(o->topk_w + (size_t)t * K, wfin, sizeof(float) * K);
+      if (o->gap) o->gap[t] = gap;
+    }
+    free(xd); free(n1); free(n2); free(moe); free(y); free(dn); free(hv);
+    free(xin); free(r); free(logits); free(probs); free(idx); free(wren); free(wfin);
+  }
+  return bad ? -1 : 0;
+}
+
+/* Slots sorted by (expert, token): the gather that precedes each expert's MLP and the scatter
+ * back ([MoE] "The architecture": the experts' sparse gather/scatter loop), as a counting sort. */
+int moe_oracle_permute(int T, int K, int E, const int32_t* topk_idx, const float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, float* w_sorted,
+                       int32_t* slot_pos) {
+  if (T < 0 || K < 1 || E < 1 || (T > 0 && !topk_idx) || !counts || !offsets) return -1;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (long s = 0; s < (long)T * K; ++s) {
+    int e = topk_idx[s];
+    if (e < 0 || e >= E) return -1;
+    counts[e] += 1;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* next = malloc(sizeof(int32_t) * E);
+  if (!next) return -1;
+  for (int e = 0; e < E; ++e) next[e] = offsets[e];
+  /* Tokens ascending, so within one expert the tokens ascend. */
+  for (int t = 0; t < T; ++t) {
+    for (int k = 0; k < K; ++k) {
+      int e = topk_idx[(size_t)t * K + k];
+      int pos = next[e]++;
+      if (perm) perm[pos] = t;
+      if (w_sorted && topk_w) w_sorted[pos] = topk_w[(size_t)t * K + k];
+      if (slot_pos) slot_pos[(size_t)t * K + k] = pos;
+    }
+  }
+  free(next);
+  return 0;
+}
+
+void moe_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int moe_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
