@@ -1,0 +1,228 @@
+"""ctypes binding of the C ABI in include/moe_ffn.h (argument marshalling only).
+
+The functions keep the C names and take plain integers for device pointers and streams. ``MoeFFN``
+is a small convenience wrapper that takes torch tensors (torch supplies device memory and the
+stream; every step of the block runs in the library's kernels). Loading fails loudly when the
+library has not been built: there is no fallback.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe_ffn.so")
+
+MOE_FFN_OK = 0
+MOE_FFN_EINVAL = -1
+MOE_FFN_EALIGN = -2
+MOE_FFN_ETOOBIG = -3
+MOE_FFN_EARCH = -4
+MOE_FFN_ECUDA = -5
+MOE_FFN_EDEVICE = -6
+MOE_FFN_MOE_ONLY = 0
+MOE_FFN_FULL_LAYER = 1
+HIDDEN, N_EXPERTS, TOP_K, MOE_INTER, DENSE_INTER = 2816, 128, 8, 704, 2112
+KERNEL_NAMES = ("router_logits", "route_topk", "route_scatter", "gate_up_gemm", "down_gemm", "combine")
+
+_vp = ctypes.c_void_p
+
+
+class moe_ffn_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("moe_inter", ctypes.c_int), ("dense_inter", ctypes.c_int), ("mode", ctypes.c_int),
+                ("max_tokens", ctypes.c_int), ("eps", ctypes.c_float), ("router_scale", ctypes.c_float)]
+
+
+WEIGHT_FIELDS = ("router_w", "router_norm_w", "per_expert_scale", "gate_up", "down", "dense_gate", "dense_up",
+                 "dense_down", "pre_ff_ln", "pre_ff_ln_2", "post_ff_ln_1", "post_ff_ln_2", "post_ff_ln")
+
+
+class moe_ffn_weights(ctypes.Structure):
+    _fields_ = [(f, _vp) for f in WEIGHT_FIELDS] + [("layer_scalar", ctypes.c_float)]
+
+
+VIEW_FIELDS = ("logits", "topk_idx", "topk_w", "gap", "counts", "offsets", "perm", "w_sorted", "slot_pos", "n1",
+               "n2", "h", "h_dense", "y", "d")
+
+
+class moe_ffn_views(ctypes.Structure):
+    _fields_ = [(f, _vp) for f in VIEW_FIELDS] + [("T", ctypes.c_int)]
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded CUDA library. Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmoe_ffn.so is not built (run __graft_entry__.build() or "
+                               "python mixture_experts_ffn_router_gb300/build.py)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.moe_ffn_workspace_bytes.restype = ctypes.c_size_t
+        L.moe_ffn_workspace_bytes.argtypes = [ctypes.POINTER(moe_ffn_config)]
+        L.moe_ffn_init.restype = ctypes.c_int
+        L.moe_ffn_init.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(moe_ffn_config), _vp, ctypes.c_size_t,
+                                   ctypes.c_int]
+        L.moe_ffn_forward.restype = ctypes.c_int
+        L.moe_ffn_forward.argtypes = [_vp, _vp, ctypes.c_int, ctypes.POINTER(moe_ffn_weights), _vp, _vp]
+        L.moe_ffn_workspace_view.restype = ctypes.c_int
+        L.moe_ffn_workspace_view.argtypes = [_vp, ctypes.POINTER(moe_ffn_views)]
+        L.moe_ffn_device_status.restype = ctypes.c_int
+        L.moe_ffn_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.moe_ffn_set_kernel_events.restype = ctypes.c_int
+        L.moe_ffn_set_kernel_events.argtypes = [_vp, ctypes.c_int, _vp, _vp]
+        L.moe_ffn_kernels_per_forward.restype = ctypes.c_int
+        L.moe_ffn_kernels_per_forward.argtypes = [_vp, ctypes.c_int]
+        L.moe_ffn_status_string.restype = ctypes.c_char_p
+        L.moe_ffn_status_string.argtypes = [ctypes.c_int]
+        L.moe_ffn_destroy.restype = None
+        L.moe_ffn_destroy.argtypes = [_vp]
+        _LIB = L
+    return _LIB
+
+
+class MoeFFNError(RuntimeError):
+    def __init__(self, call, status):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (call, moe_ffn_status_string(status), status))
+
+
+def _check(call, status):
+    if status != MOE_FFN_OK:
+        raise MoeFFNError(call, status)
+    return status
+
+
+# ------------------------------------------------------------------ the C entry points
+
+def moe_ffn_status_string(status: int) -> str:
+    return lib().moe_ffn_status_string(int(status)).decode()
+
+
+def make_config(mode: int, max_tokens: int, eps: float = 1e-6, router_scale: float = HIDDEN ** -0.5) -> moe_ffn_config:
+    return moe_ffn_config(HIDDEN, N_EXPERTS, TOP_K, MOE_INTER, DENSE_INTER, int(mode), int(max_tokens),
+                          float(eps), float(router_scale))
+
+
+def moe_ffn_workspace_bytes(cfg: moe_ffn_config) -> int:
+    return lib().moe_ffn_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_ffn_init(cfg: moe_ffn_config, workspace: int, workspace_bytes: int, device: int) -> int:
+    """Returns the context handle (an int)."""
+    h = _vp()
+    _check("moe_ffn_init", lib().moe_ffn_init(ctypes.byref(h), ctypes.byref(cfg), _vp(workspace),
+                                               workspace_bytes, int(device)))
+    return h.value
+
+
+def moe_ffn_forward(ctx: int, x: int, T: int, weights: moe_ffn_weights, out: int, stream: int) -> int:
+    return lib().moe_ffn_forward(_vp(ctx), _vp(x), int(T), ctypes.byref(weights), _vp(out), _vp(stream))
+
+
+def moe_ffn_workspace_view(ctx: int) -> moe_ffn_views:
+    v = moe_ffn_views()
+    _check("moe_ffn_workspace_view", lib().moe_ffn_workspace_view(_vp(ctx), ctypes.byref(v)))
+    return v
+
+
+def moe_ffn_device_status(ctx: int, stream: int):
+    w = ctypes.c_uint32(0)
+    rc = lib().moe_ffn_device_status(_vp(ctx), _vp(stream), ctypes.byref(w))
+    return rc, w.value
+
+
+def moe_ffn_set_kernel_events(ctx: int, kernel: int, start: int, stop: int) -> int:
+    return lib().moe_ffn_set_kernel_events(_vp(ctx), int(kernel), _vp(start), _vp(stop))
+
+
+def moe_ffn_kernels_per_forward(ctx: int, T: int) -> int:
+    return lib().moe_ffn_kernels_per_forward(_vp(ctx), int(T))
+
+
+def moe_ffn_destroy(ctx: int) -> None:
+    lib().moe_ffn_destroy(_vp(ctx))
+
+
+# ------------------------------------------------------------------ torch convenience layer
+
+def weights_struct(w: dict) -> moe_ffn_weights:
+    """A moe_ffn_weights whose fields point at the CUDA tensors of ``w`` (absent fields are NULL)."""
+    s = moe_ffn_weights()
+    for f in WEIGHT_FIELDS:
+        t = w.get(f)
+        if t is not None:
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("weight %s must be a contiguous CUDA tensor" % f)
+            setattr(s, f, t.data_ptr())
+    if "layer_scalar" not in w:
+        raise ValueError("layer_scalar is required")
+    s.layer_scalar = float(w["layer_scalar"])
+    return s
+
+
+class MoeFFN:
+    """One context with its workspace (a torch uint8 tensor on the device)."""
+
+    def __init__(self, mode: int, max_tokens: int, device: int = 0, workspace=None):
+        import torch
+        self.cfg = make_config(mode, max_tokens)
+        self.nbytes = moe_ffn_workspace_bytes(self.cfg)
+        if self.nbytes == 0:
+            raise ValueError("invalid configuration")
+        self.device = int(device)
+        if workspace is None:
+            workspace = torch.empty(self.nbytes, dtype=torch.uint8, device="cuda:%d" % self.device)
+        elif workspace.numel() < self.nbytes:
+            raise ValueError("workspace too small")
+        self.workspace = workspace
+        self.ctx = moe_ffn_init(self.cfg, workspace.data_ptr(), workspace.numel(), self.device)
+
+    def forward(self, x, weights, out=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        ws = weights if isinstance(weights, moe_ffn_weights) else weights_struct(weights)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        _check("moe_ffn_forward", moe_ffn_forward(self.ctx, x.data_ptr(), T, ws, out.data_ptr(), s))
+        return out
+
+    def views(self) -> moe_ffn_views:
+        return moe_ffn_workspace_view(self.ctx)
+
+    def status(self, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        return moe_ffn_device_status(self.ctx, s)
+
+    def close(self):
+        if self.ctx:
+            moe_ffn_destroy(self.ctx)
+            self.ctx = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def view_tensor(ptr: int, shape, dtype, device: int = 0):
+    """A torch tensor aliasing device memory at ``ptr`` (for reading the workspace views)."""
+    import torch
+    n = 1
+    for s in shape:
+        n *= s
+    if n == 0:
+        return torch.empty(shape, dtype=dtype, device="cuda:%d" % device)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+
+    class _Holder:
+        __cuda_array_interface__ = {
+            "shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3, "strides": None,
+        }
+
+    raw = torch.as_tensor(_Holder(), device="cuda:%d" % device)
+    return raw.view(dtype).view(*shape)

@@ -1,0 +1,101 @@
+// internal.h — declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int H = 2816;   // hidden
+constexpr int E = 128;    // experts
+constexpr int K = 8;      // experts per token
+constexpr int I = 704;    // expert intermediate width
+constexpr int D = 2112;   // shared-MLP intermediate width
+
+// Router-logit kernel tiling: 32 tokens x 64 experts per CTA, K split into `ks` equal parts.
+constexpr int kRouterTok = 32;
+constexpr int kRouterExp = 64;
+constexpr int kRouterKc = 64;
+// Token-scatter kernel: 256 tokens per CTA (8 warps of 32).
+constexpr int kScatterTok = 256;
+// Combine kernel: one CTA per token, 352 threads x 8 features.
+constexpr int kCombineThreads = 352;
+
+// Device pointers of one forward's intermediates, carved from the caller's workspace.
+struct Buffers {
+  float* logits_part;   // [ks, T, 128]
+  float* logits;        // [Tm, 128]
+  int32_t* topk_idx;    // [Tm, 8]
+  float* topk_w;        // [Tm, 8]
+  float* gap;           // [Tm]
+  int32_t* hist;        // [kMaxRouteBlocks, 128] per-CTA expert counts of the top-k kernel
+  int32_t* base;        // [kMaxRouteBlocks, 128] first sorted position of each (CTA, expert)
+  int32_t* counts;      // [128]
+  int32_t* offsets;     // [129]
+  int32_t* n_exp_tiles; // [1]
+  int32_t* done_ctr;    // [1]
+  int4* exp_tiles;      // [max_tiles] (expert, first sorted row, rows, 0)
+  int32_t* perm;        // [S]
+  float* w_sorted;      // [S]
+  int32_t* slot_pos;    // [Tm, 8]
+  uint16_t* n1;         // [Tm, 2816]
+  uint16_t* n2;         // [Tm, 2816]
+  uint16_t* h;          // [S, 704]
+  uint16_t* h_dense;    // [Tm, 2112]
+  float* y;             // [S, 2816]
+  float* d;             // [Tm, 2816]
+  unsigned int* status; // [1]
+  int max_tiles;
+};
+
+constexpr int kMaxRouteBlocks = 256;
+
+struct RouteParams {
+  const uint16_t* x;
+  const float* router_w;
+  const float* router_norm_w;
+  const float* per_expert_scale;
+  const float* pre_ff_ln;
+  const float* pre_ff_ln_2;
+  int T;
+  int ks;               // K splits of the router projection
+  int tpw;              // tokens per warp in the top-k kernel
+  int bn;               // token-tile width of the grouped GEMMs
+  int full_layer;
+  float eps;
+  float router_scale;
+};
+
+struct CombineParams {
+  const uint16_t* x;
+  const float* post_ff_ln_1;
+  const float* post_ff_ln_2;
+  const float* post_ff_ln;
+  float layer_scalar;
+  uint16_t* out;
+  int T;
+  int full_layer;
+  float eps;
+};
+
+// Maps of one grouped GEMM launch. For gate_up: a_exp = gate_up rows, a_dense0/1 = dense gate/up,
+// b_exp = n2 (gather), b_dense = n1 (gather). For down: a_exp = down rows, a_dense0 = dense down,
+// b_exp = h (gather), b_dense = h_dense (gather).
+struct GemmMaps {
+  CUtensorMap a_exp, a_dense0, a_dense1, b_exp, b_dense;
+};
+
+cudaError_t launch_router_logits(const RouteParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_route_scatter(const RouteParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, const Buffers& b, cudaStream_t s);
+
+// Grouped GEMMs (gemm.cu). `grid` CTAs persistent over the device-side tile list.
+cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+                           cudaStream_t s);
+cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+                        cudaStream_t s);
+cudaError_t gemm_set_smem_limits();
+
+}  // namespace moe

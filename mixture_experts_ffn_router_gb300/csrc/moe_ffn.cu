@@ -1,0 +1,424 @@
+// moe_ffn.cu — host side of the library: the C ABI of include/moe_ffn.h, workspace layout,
+// TMA tensor maps and the launch sequence of one forward.
+//
+// One forward of T tokens queues six kernels on the caller's stream, in this order:
+//   0 router logits   fp32 partial projections of the router ("The architecture": own RMSNorm,
+//                     a scale, softmax over 128 experts in fp32)
+//   1 top-k           RMS of x, the pre-norms, softmax, top-8, renormalise, per_expert_scale,
+//                     per-CTA expert counts -> offsets, bases and the token-tile list
+//   2 scatter         stable counting-sort scatter of the 8T slots by expert
+//   3 gate_up GEMM    tcgen05 grouped GEMM, h = gelu_tanh(gate) * up (experts + shared MLP)
+//   4 down GEMM       tcgen05 grouped GEMM, y = w * down(h) (experts), d = down(h) (shared MLP)
+//   5 combine         per token: sum of its 8 y rows, the post-norms, residual, layer_scalar
+// Nothing is read back to the host; the GEMMs size their work from device-side counts.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/moe_ffn.h"
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows, cols] row-major, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Largest split of the router projection that keeps the router grid near two CTAs per SM of a
+// 152-SM part; a fixed rule so the workspace size does not depend on the device.
+int choose_ks(int T) {
+  static const int opts[] = {44, 22, 11, 4, 2, 1};
+  const int tiles = ((T + kRouterTok - 1) / kRouterTok) * (E / kRouterExp);
+  for (int o : opts)
+    if (tiles * o <= 352) return o;
+  return 1;
+}
+constexpr size_t kPartRowsSmall = 5632;  // max ks * T over the T where ks > 1
+
+int choose_tpw(int T) {
+  int tpw = 1;
+  while ((T + 8 * tpw - 1) / (8 * tpw) > kMaxRouteBlocks && tpw < 32) tpw *= 2;
+  return tpw;
+}
+
+int choose_bn(int T) {
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  if (T <= 1024) return 128;
+  return 256;
+}
+
+struct Layout {
+  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, n_exp_tiles, done_ctr, exp_tiles,
+      perm, w_sorted, slot_pos, n1, n2, h, h_dense, y, d, status, total;
+  int max_tiles;
+};
+
+Layout make_layout(const moe_ffn_config& c) {
+  const size_t Tm = static_cast<size_t>(c.max_tokens);
+  const size_t S = Tm * K;
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t part_rows = Tm > kPartRowsSmall ? Tm : kPartRowsSmall;
+  L.max_tiles = static_cast<int>(S / 32 + E);
+  L.logits_part = take(part_rows * E * 4);
+  L.logits = take(Tm * E * 4);
+  L.topk_idx = take(Tm * K * 4);
+  L.topk_w = take(Tm * K * 4);
+  L.gap = take(Tm * 4);
+  L.hist = take(static_cast<size_t>(kMaxRouteBlocks) * E * 4);
+  L.base = take(static_cast<size_t>(kMaxRouteBlocks) * E * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.n_exp_tiles = take(4);
+  L.done_ctr = take(4);
+  L.status = take(4);
+  L.exp_tiles = take(static_cast<size_t>(L.max_tiles) * 16);
+  L.perm = take(S * 4);
+  L.w_sorted = take(S * 4);
+  L.slot_pos = take(S * 4);
+  L.n1 = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * H * 2 : 0);
+  L.n2 = take(Tm * H * 2);
+  L.h = take(S * I * 2);
+  L.h_dense = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * D * 2 : 0);
+  L.y = take(S * H * 4);
+  L.d = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * H * 4 : 0);
+  L.total = o;
+  return L;
+}
+
+bool config_ok(const moe_ffn_config* c) {
+  return c && c->hidden == H && c->n_experts == E && c->top_k == K && c->moe_inter == I && c->dense_inter == D &&
+         (c->mode == MOE_FFN_MOE_ONLY || c->mode == MOE_FFN_FULL_LAYER) && c->max_tokens >= 1 &&
+         c->max_tokens <= MOE_FFN_MAX_TOKENS_LIMIT && c->eps > 0.0f && c->router_scale > 0.0f;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct moe_ffn_ctx {
+  moe_ffn_config cfg;
+  int device;
+  int num_sms;
+  uint8_t* ws;
+  size_t ws_bytes;
+  Buffers buf;
+  CUtensorMap map_n1, map_n2, map_h, map_hd;
+  // weight maps, re-encoded when the weight pointers change
+  const void* cached_gate_up;
+  const void* cached_down;
+  const void* cached_dense_gate;
+  const void* cached_dense_up;
+  const void* cached_dense_down;
+  CUtensorMap map_gate_up, map_down, map_dense_gate, map_dense_up, map_dense_down;
+  cudaEvent_t ev_start[6];
+  cudaEvent_t ev_stop[6];
+  int last_T;
+};
+
+extern "C" {
+
+const char* moe_ffn_status_string(int status) {
+  switch (status) {
+    case MOE_FFN_OK: return "ok";
+    case MOE_FFN_EINVAL: return "invalid argument";
+    case MOE_FFN_EALIGN: return "device pointer not 16-byte aligned";
+    case MOE_FFN_ETOOBIG: return "size above the context's limit";
+    case MOE_FFN_EARCH: return "device is not sm_103 (GB300)";
+    case MOE_FFN_ECUDA: return "CUDA call failed";
+    case MOE_FFN_EDEVICE: return "a kernel reported a bounded-wait timeout or a bad index";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_ffn_workspace_bytes(const moe_ffn_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return make_layout(*cfg).total;
+}
+
+int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, size_t workspace_bytes,
+                 int device) {
+  if (!out) return MOE_FFN_EINVAL;
+  *out = nullptr;
+  if (!config_ok(cfg) || !workspace) return MOE_FFN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_FFN_EALIGN;
+  const Layout L = make_layout(*cfg);
+  if (workspace_bytes < L.total) return MOE_FFN_ETOOBIG;
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_FFN_ECUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return MOE_FFN_ECUDA;
+  if (major != 10 || minor != 3) return MOE_FFN_EARCH;
+  if (!get_encode()) return MOE_FFN_ECUDA;
+  if (gemm_set_smem_limits() != cudaSuccess) return MOE_FFN_ECUDA;
+
+  moe_ffn_ctx* c = new (std::nothrow) moe_ffn_ctx();
+  if (!c) return MOE_FFN_ECUDA;
+  c->cfg = *cfg;
+  c->device = device;
+  c->num_sms = sms;
+  c->ws = static_cast<uint8_t*>(workspace);
+  c->ws_bytes = workspace_bytes;
+  uint8_t* w = c->ws;
+  Buffers& b = c->buf;
+  b.logits_part = reinterpret_cast<float*>(w + L.logits_part);
+  b.logits = reinterpret_cast<float*>(w + L.logits);
+  b.topk_idx = reinterpret_cast<int32_t*>(w + L.topk_idx);
+  b.topk_w = reinterpret_cast<float*>(w + L.topk_w);
+  b.gap = reinterpret_cast<float*>(w + L.gap);
+  b.hist = reinterpret_cast<int32_t*>(w + L.hist);
+  b.base = reinterpret_cast<int32_t*>(w + L.base);
+  b.counts = reinterpret_cast<int32_t*>(w + L.counts);
+  b.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  b.n_exp_tiles = reinterpret_cast<int32_t*>(w + L.n_exp_tiles);
+  b.done_ctr = reinterpret_cast<int32_t*>(w + L.done_ctr);
+  b.status = reinterpret_cast<unsigned int*>(w + L.status);
+  b.exp_tiles = reinterpret_cast<int4*>(w + L.exp_tiles);
+  b.perm = reinterpret_cast<int32_t*>(w + L.perm);
+  b.w_sorted = reinterpret_cast<float*>(w + L.w_sorted);
+  b.slot_pos = reinterpret_cast<int32_t*>(w + L.slot_pos);
+  b.n1 = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<uint16_t*>(w + L.n1) : nullptr;
+  b.n2 = reinterpret_cast<uint16_t*>(w + L.n2);
+  b.h = reinterpret_cast<uint16_t*>(w + L.h);
+  b.h_dense = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<uint16_t*>(w + L.h_dense) : nullptr;
+  b.y = reinterpret_cast<float*>(w + L.y);
+  b.d = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<float*>(w + L.d) : nullptr;
+  b.max_tiles = L.max_tiles;
+
+  const uint64_t Tm = static_cast<uint64_t>(cfg->max_tokens);
+  bool ok = encode_bf16(&c->map_n2, b.n2, Tm, H, 1) && encode_bf16(&c->map_h, b.h, Tm * K, I, 1);
+  if (cfg->mode == MOE_FFN_FULL_LAYER)
+    ok = ok && encode_bf16(&c->map_n1, b.n1, Tm, H, 1) && encode_bf16(&c->map_hd, b.h_dense, Tm, D, 1);
+  else {
+    c->map_n1 = c->map_n2;
+    c->map_hd = c->map_h;
+  }
+  // The small control words start at zero; the kernels keep them consistent afterwards.
+  if (!ok || cudaMemset(w + L.hist, 0, L.exp_tiles - L.hist) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    delete c;
+    return MOE_FFN_ECUDA;
+  }
+  *out = c;
+  return MOE_FFN_OK;
+}
+
+void moe_ffn_destroy(moe_ffn_ctx* ctx) { delete ctx; }
+
+static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
+  const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
+  if (!w->router_w || !w->router_norm_w || !w->per_expert_scale || !w->gate_up || !w->down) return MOE_FFN_EINVAL;
+  if (full && (!w->dense_gate || !w->dense_up || !w->dense_down || !w->pre_ff_ln || !w->pre_ff_ln_2 ||
+               !w->post_ff_ln_1 || !w->post_ff_ln_2 || !w->post_ff_ln))
+    return MOE_FFN_EINVAL;
+  const void* ps[] = {w->router_w, w->router_norm_w, w->per_expert_scale, w->gate_up, w->down};
+  for (const void* p : ps)
+    if (!aligned16(p)) return MOE_FFN_EALIGN;
+  if (full) {
+    const void* pf[] = {w->dense_gate, w->dense_up, w->dense_down, w->pre_ff_ln, w->pre_ff_ln_2,
+                        w->post_ff_ln_1, w->post_ff_ln_2, w->post_ff_ln};
+    for (const void* p : pf)
+      if (!aligned16(p)) return MOE_FFN_EALIGN;
+  }
+  const bool same = c->cached_gate_up == w->gate_up && c->cached_down == w->down &&
+                    (!full || (c->cached_dense_gate == w->dense_gate && c->cached_dense_up == w->dense_up &&
+                               c->cached_dense_down == w->dense_down));
+  if (same) return MOE_FFN_OK;
+  bool ok = encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 16) &&
+            encode_bf16(&c->map_down, w->down, static_cast<uint64_t>(E) * H, I, 128);
+  if (full)
+    ok = ok && encode_bf16(&c->map_dense_gate, w->dense_gate, D, H, 16) &&
+         encode_bf16(&c->map_dense_up, w->dense_up, D, H, 16) &&
+         encode_bf16(&c->map_dense_down, w->dense_down, H, D, 128);
+  else {
+    c->map_dense_gate = c->map_gate_up;
+    c->map_dense_up = c->map_gate_up;
+    c->map_dense_down = c->map_down;
+  }
+  if (!ok) {
+    c->cached_gate_up = nullptr;
+    return MOE_FFN_ECUDA;
+  }
+  c->cached_gate_up = w->gate_up;
+  c->cached_down = w->down;
+  c->cached_dense_gate = w->dense_gate;
+  c->cached_dense_up = w->dense_up;
+  c->cached_dense_down = w->dense_down;
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights* w, void* out, void* stream) {
+  if (!c || !w) return MOE_FFN_EINVAL;
+  if (T < 0) return MOE_FFN_EINVAL;
+  if (T > c->cfg.max_tokens) return MOE_FFN_ETOOBIG;
+  if (T == 0) return MOE_FFN_OK;
+  if (!x || !out) return MOE_FFN_EINVAL;
+  if (!aligned16(x) || !aligned16(out)) return MOE_FFN_EALIGN;
+  const size_t io_bytes = static_cast<size_t>(T) * H * 2;
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  uint8_t* ob = static_cast<uint8_t*>(out);
+  if ((ob < xb + io_bytes && xb < ob + io_bytes) || (ob < c->ws + c->ws_bytes && c->ws < ob + io_bytes))
+    return MOE_FFN_EINVAL;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_FFN_ECUDA;
+  if (cur != c->device && cudaSetDevice(c->device) != cudaSuccess) return MOE_FFN_ECUDA;
+  int rc = prepare_weights(c, w);
+  if (rc != MOE_FFN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
+
+  RouteParams rp;
+  rp.x = static_cast<const uint16_t*>(x);
+  rp.router_w = w->router_w;
+  rp.router_norm_w = w->router_norm_w;
+  rp.per_expert_scale = w->per_expert_scale;
+  rp.pre_ff_ln = w->pre_ff_ln;
+  rp.pre_ff_ln_2 = w->pre_ff_ln_2;
+  rp.T = T;
+  rp.ks = choose_ks(T);
+  rp.tpw = choose_tpw(T);
+  rp.bn = choose_bn(T);
+  rp.full_layer = full ? 1 : 0;
+  rp.eps = c->cfg.eps;
+  rp.router_scale = c->cfg.router_scale;
+
+  CombineParams cp;
+  cp.x = rp.x;
+  cp.post_ff_ln_1 = w->post_ff_ln_1;
+  cp.post_ff_ln_2 = w->post_ff_ln_2;
+  cp.post_ff_ln = w->post_ff_ln;
+  cp.layer_scalar = w->layer_scalar;
+  cp.out = static_cast<uint16_t*>(out);
+  cp.T = T;
+  cp.full_layer = rp.full_layer;
+  cp.eps = c->cfg.eps;
+
+  GemmMaps gu, dn;
+  gu.a_exp = c->map_gate_up;
+  gu.a_dense0 = c->map_dense_gate;
+  gu.a_dense1 = c->map_dense_up;
+  gu.b_exp = c->map_n2;
+  gu.b_dense = c->map_n1;
+  dn.a_exp = c->map_down;
+  dn.a_dense0 = c->map_dense_down;
+  dn.a_dense1 = c->map_dense_down;
+  dn.b_exp = c->map_h;
+  dn.b_dense = c->map_hd;
+
+  // Persistent GEMM grids: at most one CTA per SM, and no more than an upper bound of the items.
+  const int S = T * K;
+  const int bn = rp.bn;
+  const int ub_tiles = (S < E ? S : E) + S / bn;
+  const int nd = full ? (T + bn - 1) / bn : 0;
+  const long items_gu = static_cast<long>(ub_tiles) * (I / 64) + static_cast<long>(nd) * (D / 64);
+  const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
+  const int grid_gu = static_cast<int>(items_gu < c->num_sms ? items_gu : c->num_sms);
+  const int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
+
+  cudaError_t e = cudaSuccess;
+  for (int k = 0; k < 6 && e == cudaSuccess; ++k) {
+    if (c->ev_start[k]) e = cudaEventRecord(c->ev_start[k], s);
+    if (e != cudaSuccess) break;
+    switch (k) {
+      case 0: e = launch_router_logits(rp, c->buf, s); break;
+      case 1: e = launch_route_topk(rp, c->buf, s); break;
+      case 2: e = launch_route_scatter(rp, c->buf, s); break;
+      case 3: e = launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s); break;
+      case 4: e = launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s); break;
+      case 5: e = launch_combine(cp, c->buf, s); break;
+    }
+    if (e == cudaSuccess && c->ev_stop[k]) e = cudaEventRecord(c->ev_stop[k], s);
+  }
+  if (e != cudaSuccess) return MOE_FFN_ECUDA;
+  c->last_T = T;
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_workspace_view(const moe_ffn_ctx* c, moe_ffn_views* v) {
+  if (!c || !v) return MOE_FFN_EINVAL;
+  const Buffers& b = c->buf;
+  v->logits = b.logits;
+  v->topk_idx = b.topk_idx;
+  v->topk_w = b.topk_w;
+  v->gap = b.gap;
+  v->counts = b.counts;
+  v->offsets = b.offsets;
+  v->perm = b.perm;
+  v->w_sorted = b.w_sorted;
+  v->slot_pos = b.slot_pos;
+  v->n1 = b.n1;
+  v->n2 = b.n2;
+  v->h = b.h;
+  v->h_dense = b.h_dense;
+  v->y = b.y;
+  v->d = b.d;
+  v->T = c->last_T;
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_device_status(moe_ffn_ctx* c, void* stream, uint32_t* word) {
+  if (!c) return MOE_FFN_EINVAL;
+  if (cudaSetDevice(c->device) != cudaSuccess) return MOE_FFN_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_FFN_ECUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, c->buf.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_FFN_ECUDA;
+  if (v != 0 && cudaMemset(c->buf.status, 0, 4) != cudaSuccess) return MOE_FFN_ECUDA;
+  if (word) *word = v;
+  return v ? MOE_FFN_EDEVICE : MOE_FFN_OK;
+}
+
+int moe_ffn_set_kernel_events(moe_ffn_ctx* c, int kernel, void* start, void* stop) {
+  if (!c || kernel < 0 || kernel >= 6) return MOE_FFN_EINVAL;
+  if ((start == nullptr) != (stop == nullptr)) return MOE_FFN_EINVAL;
+  c->ev_start[kernel] = static_cast<cudaEvent_t>(start);
+  c->ev_stop[kernel] = static_cast<cudaEvent_t>(stop);
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_kernels_per_forward(const moe_ffn_ctx* c, int T) {
+  if (!c || T < 0) return MOE_FFN_EINVAL;
+  return T == 0 ? 0 : 6;
+}
+
+}  // extern "C"

@@ -1,0 +1,534 @@
+// route.cu — the CUDA-core kernels of the block: router projection, top-k with the pre-norms,
+// the counting-sort scatter of token slots by expert, and the combine with the post-norms.
+//
+// What they compute follows "Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS Inferentia2 —
+// where every rank weighted the wrong experts", section "The architecture: a dual-path FFN nobody
+// warned me about": the router normalises its input with its own RMSNorm, multiplies by a scale
+// and per-expert weights, takes a softmax over 128 experts in fp32, keeps the top 8, renormalises
+// them to sum 1 and multiplies by per_expert_scale; the expert outputs are gathered back to their
+// tokens and, with the shared MLP, pass through the feed-forward norms, the residual add and
+// layer_scalar ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", §4.6).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------------------------------
+// K1: partial router logits. part[ks][t][e] = sum over the ks-th slice of h of
+// x[t,h] * (1 + router_norm_w[h]) * W_r[e,h]. The RMS factor and the scalar scale are applied
+// after the split sum, in the top-k kernel. fp32 FFMA throughout: the top-8 choice must be taken
+// on fp32 logits.
+__global__ void __launch_bounds__(256) router_logits_kernel(RouteParams p, Buffers b) {
+  __shared__ float xs[kRouterTok][kRouterKc + 1];
+  __shared__ float ws[kRouterExp][kRouterKc + 1];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * kRouterTok, e0 = blockIdx.y * kRouterExp, ks = blockIdx.z;
+  const int ks_len = H / p.ks;
+  const int kbeg = ks * ks_len;
+  const int ty = tid >> 4, tx = tid & 15;
+  pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) *b.done_ctr = 0;
+
+  float acc[2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+  for (int kc = kbeg; kc < kbeg + ks_len; kc += kRouterKc) {
+    {  // x tile: 32 tokens x 64 columns, 8 bf16 per thread
+      const int r = tid >> 3, c = (tid & 7) * 8;
+      const int t = t0 + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < p.T) v = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + kc + c);
+      const float4 g0 = *reinterpret_cast<const float4*>(p.router_norm_w + kc + c);
+      const float4 g1 = *reinterpret_cast<const float4*>(p.router_norm_w + kc + c + 4);
+      xs[r][c + 0] = bf16_lo(v.x) * (1.0f + g0.x);
+      xs[r][c + 1] = bf16_hi(v.x) * (1.0f + g0.y);
+      xs[r][c + 2] = bf16_lo(v.y) * (1.0f + g0.z);
+      xs[r][c + 3] = bf16_hi(v.y) * (1.0f + g0.w);
+      xs[r][c + 4] = bf16_lo(v.z) * (1.0f + g1.x);
+      xs[r][c + 5] = bf16_hi(v.z) * (1.0f + g1.y);
+      xs[r][c + 6] = bf16_lo(v.w) * (1.0f + g1.z);
+      xs[r][c + 7] = bf16_hi(v.w) * (1.0f + g1.w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // W tile: 64 experts x 64 columns, 16 floats per thread
+      const int idx = tid + 256 * i;
+      const int r = idx >> 4, c = (idx & 15) * 4;
+      const float4 v = *reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e0 + r) * H + kc + c);
+      ws[r][c + 0] = v.x;
+      ws[r][c + 1] = v.y;
+      ws[r][c + 2] = v.z;
+      ws[r][c + 3] = v.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kRouterKc; ++kk) {
+      const float a0 = xs[2 * ty][kk], a1 = xs[2 * ty + 1][kk];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float w = ws[tx + 16 * j][kk];
+        acc[0][j] = fmaf(a0, w, acc[0][j]);
+        acc[1][j] = fmaf(a1, w, acc[1][j]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = t0 + 2 * ty + i;
+    if (t < p.T) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        b.logits_part[(static_cast<size_t>(ks) * p.T + t) * E + e0 + tx + 16 * j] = acc[i][j];
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// Warp arg-max over (logit, expert) pairs: larger logit first, lower expert id on equal logits.
+struct Cand {
+  float l;
+  float p;
+  int e;
+};
+
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  return a.l > b.l || (a.l == b.l && a.e < b.e);
+}
+
+__device__ __forceinline__ Cand warp_argmax(Cand c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand d;
+    d.l = __shfl_xor_sync(0xffffffffu, c.l, o);
+    d.p = __shfl_xor_sync(0xffffffffu, c.p, o);
+    d.e = __shfl_xor_sync(0xffffffffu, c.e, o);
+    if (better(d, c)) c = d;
+  }
+  return c;
+}
+
+// ------------------------------------------------------------------------------------------
+// K2: one warp per token. RMS of x; the two pre-norms (full layer) or a copy of x (experts
+// only) as the expert input; logits = rms * scale * sum of the partials; fp32 softmax; top-8 by
+// logit with the 9th for the gap; renormalise, times per_expert_scale; slots listed in ascending
+// expert id. Each CTA counts its slots per expert; the last CTA to finish turns the counts into
+// expert offsets, per-CTA base positions and the grouped GEMMs' token-tile list.
+__global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers b) {
+  __shared__ int hist_s[E];
+  __shared__ int part_s[2][E];
+  __shared__ int scan_s[E + 1];
+  __shared__ int tscan_s[E + 1];
+  __shared__ int is_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < E) hist_s[tid] = 0;
+  pdl_wait();
+  __syncthreads();
+
+  const int tb = 8 * p.tpw;
+  for (int i = 0; i < p.tpw; ++i) {
+    const int t = blockIdx.x * tb + warp * p.tpw + i;
+    if (t >= p.T) break;
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
+    uint4 xv[11];
+    float ss = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 11; ++c) {
+      xv[c] = xr[lane + 32 * c];
+      const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = bf16_lo(w4[j]), bb = bf16_hi(w4[j]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(bb, bb, ss);
+      }
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + p.eps);
+
+    // Expert-branch input n2 and dense-branch input n1.
+    uint4* n2r = reinterpret_cast<uint4*>(b.n2 + static_cast<size_t>(t) * H);
+    if (p.full_layer) {
+      uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
+#pragma unroll
+      for (int c = 0; c < 11; ++c) {
+        const int col = (lane + 32 * c) * 8;
+        const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+        const float4 a0 = *reinterpret_cast<const float4*>(p.pre_ff_ln + col);
+        const float4 a1 = *reinterpret_cast<const float4*>(p.pre_ff_ln + col + 4);
+        const float4 c0 = *reinterpret_cast<const float4*>(p.pre_ff_ln_2 + col);
+        const float4 c1 = *reinterpret_cast<const float4*>(p.pre_ff_ln_2 + col + 4);
+        const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float g2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t o1[4], o2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
+          o1[j] = pack_bf16(lo * (1.0f + g1[2 * j]), hi * (1.0f + g1[2 * j + 1]));
+          o2[j] = pack_bf16(lo * (1.0f + g2[2 * j]), hi * (1.0f + g2[2 * j + 1]));
+        }
+        n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        n2r[lane + 32 * c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = xv[c];
+    }
+
+    // Logits: expert e = lane + 32 j, partial sums added in ascending split order.
+    float lg[4], pr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = lane + 32 * j;
+      float z = 0.0f;
+      for (int s = 0; s < p.ks; ++s) z += b.logits_part[(static_cast<size_t>(s) * p.T + t) * E + e];
+      lg[j] = z * inv * p.router_scale;
+      b.logits[static_cast<size_t>(t) * E + e] = lg[j];
+    }
+    const float m = warp_max(fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3])));
+    float zsum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pr[j] = expf(lg[j] - m);
+      zsum += pr[j];
+    }
+    zsum = warp_sum(zsum);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pr[j] = pr[j] / zsum;
+
+    // Top-8 (and the 9th for the gap) by repeated warp arg-max.
+    unsigned taken = 0;
+    int sel_e[K];
+    float sel_p[K];
+    float l8 = 0.0f, l9 = 0.0f;
+#pragma unroll
+    for (int r = 0; r < K + 1; ++r) {
+      Cand c{-INFINITY, 0.0f, 0x7fffffff};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        Cand d{lg[j], pr[j], lane + 32 * j};
+        if (!(taken & (1u << j)) && (c.e == 0x7fffffff || better(d, c))) c = d;
+      }
+      c = warp_argmax(c);
+      if ((c.e & 31) == lane) taken |= 1u << (c.e >> 5);
+      if (r < K) {
+        sel_e[r] = c.e;
+        sel_p[r] = c.p;
+      }
+      if (r == K - 1) l8 = c.l;
+      if (r == K) l9 = c.l;
+    }
+    // Ascending expert id (odd-even transposition sort, identical in every lane).
+#pragma unroll
+    for (int pass = 0; pass < K; ++pass) {
+#pragma unroll
+      for (int j = (pass & 1); j + 1 < K; j += 2) {
+        if (sel_e[j] > sel_e[j + 1]) {
+          const int te = sel_e[j];
+          sel_e[j] = sel_e[j + 1];
+          sel_e[j + 1] = te;
+          const float tp = sel_p[j];
+          sel_p[j] = sel_p[j + 1];
+          sel_p[j + 1] = tp;
+        }
+      }
+    }
+    float psum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < K; ++j) psum += sel_p[j];
+    if (lane < K) {
+      int e = sel_e[0];
+      float pp = sel_p[0];
+#pragma unroll
+      for (int j = 1; j < K; ++j)
+        if (lane == j) {
+          e = sel_e[j];
+          pp = sel_p[j];
+        }
+      const float w = (pp / psum) * p.per_expert_scale[e];
+      b.topk_idx[static_cast<size_t>(t) * K + lane] = e;
+      b.topk_w[static_cast<size_t>(t) * K + lane] = w;
+      atomicAdd(&hist_s[e], 1);
+    }
+    if (lane == 0) b.gap[t] = l8 - l9;
+  }
+
+  // Per-CTA counts, then the last CTA to arrive builds the offsets, bases and tile list.
+  __syncthreads();
+  if (tid < E) b.hist[blockIdx.x * E + tid] = hist_s[tid];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int ticket = atomicAdd(b.done_ctr, 1);
+    is_last = (ticket == static_cast<int>(gridDim.x) - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  const int nb = gridDim.x;
+  const int e = tid & (E - 1), half = tid >> 7;
+  const int bmid = (nb + 1) / 2;
+  const int blo = half ? bmid : 0, bhi = half ? nb : bmid;
+  {
+    int s = 0;
+    for (int bb = blo; bb < bhi; ++bb) s += __ldcg(b.hist + bb * E + e);
+    part_s[half][e] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // Exclusive scans over the 128 experts of the counts and of the token-tile counts.
+    int cnt[4], nt[4];
+    int cs = 0, ts = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ee = lane * 4 + j;
+      cnt[j] = part_s[0][ee] + part_s[1][ee];
+      nt[j] = (cnt[j] + p.bn - 1) / p.bn;
+      cs += cnt[j];
+      ts += nt[j];
+    }
+    int ci = cs, ti = ts;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ci, o);
+      const int c = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) {
+        ci += a;
+        ti += c;
+      }
+    }
+    int cex = ci - cs, tex = ti - ts;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ee = lane * 4 + j;
+      scan_s[ee] = cex;
+      tscan_s[ee] = tex;
+      b.counts[ee] = cnt[j];
+      b.offsets[ee] = cex;
+      cex += cnt[j];
+      tex += nt[j];
+    }
+    if (lane == 31) {
+      scan_s[E] = cex;
+      tscan_s[E] = tex;
+      b.offsets[E] = cex;
+      if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
+      *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
+    }
+  }
+  __syncthreads();
+  {
+    // Base position of each (CTA, expert): the expert's offset plus the slots of earlier CTAs.
+    int run = scan_s[e] + (half ? part_s[0][e] : 0);
+    for (int bb = blo; bb < bhi; ++bb) {
+      const int c = __ldcg(b.hist + bb * E + e);
+      b.base[bb * E + e] = run;
+      run += c;
+    }
+  }
+  if (half == 0 && tscan_s[E] <= b.max_tiles) {
+    const int cnt = scan_s[e + 1] - scan_s[e];
+    const int nt = tscan_s[e + 1] - tscan_s[e];
+    for (int j = 0; j < nt; ++j) {
+      const int rows = min(p.bn, cnt - j * p.bn);
+      b.exp_tiles[tscan_s[e] + j] = make_int4(e, scan_s[e] + j * p.bn, rows, 0);
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// ------------------------------------------------------------------------------------------
+// K3: stable scatter of the slots. A CTA takes 256 consecutive tokens (8 warps of 32); a slot's
+// rank inside its expert is the number of earlier tokens of the CTA that chose the same expert
+// (from per-warp bit masks), on top of the base the top-k kernel computed for the CTA.
+__global__ void __launch_bounds__(256) route_scatter_kernel(RouteParams p, Buffers b) {
+  __shared__ uint32_t mask_s[8][E];
+  __shared__ int pre_s[8][E];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 8 * E; i += 256) (&mask_s[0][0])[i] = 0u;
+  pdl_wait();
+  __syncthreads();
+  const int t = blockIdx.x * kScatterTok + warp * 32 + lane;
+  const bool valid = t < p.T;
+  int ids[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    ids[k] = valid ? b.topk_idx[static_cast<size_t>(t) * K + k] : 0;
+    if (valid) {
+      if (ids[k] < 0 || ids[k] >= E) {
+        atomicOr(b.status, kStatusBadIndex);
+        ids[k] = 0;
+      } else {
+        atomicOr(&mask_s[warp][ids[k]], 1u << lane);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < E) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      pre_s[w][tid] = run;
+      run += __popc(mask_s[w][tid]);
+    }
+  }
+  __syncthreads();
+  if (!valid) return;
+  const int tb = 8 * p.tpw;
+  const int b0 = (blockIdx.x * kScatterTok) / tb;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int S = p.T * K;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int e = ids[k];
+    const int pos = b.base[b0 * E + e] + pre_s[warp][e] + __popc(mask_s[warp][e] & lt);
+    if (pos < 0 || pos >= S) {
+      atomicOr(b.status, kStatusBadIndex);
+      continue;
+    }
+    b.perm[pos] = t;
+    b.w_sorted[pos] = b.topk_w[static_cast<size_t>(t) * K + k];
+    b.slot_pos[static_cast<size_t>(t) * K + k] = pos;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// K6: one CTA per token. The expert branch is the sum of the token's 8 weighted expert outputs
+// in ascending expert id; in the full layer it is normalised by post_feedforward_layernorm_2, the
+// shared-MLP output by post_feedforward_layernorm_1, their sum by post_feedforward_layernorm, the
+// residual is added and the result multiplied by layer_scalar.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) s += red[w];
+  return s;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p, Buffers b) {
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ int pos_s[K];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int f = tid * 8;
+  pdl_wait();
+  if (tid < K) {
+    int pos = b.slot_pos[static_cast<size_t>(t) * K + tid];
+    if (pos < 0 || pos >= p.T * K) {
+      atomicOr(b.status, kStatusBadIndex);
+      pos = 0;
+    }
+    pos_s[tid] = pos;
+  }
+  __syncthreads();
+  float moe[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) moe[j] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const float* yr = b.y + static_cast<size_t>(pos_s[k]) * H + f;
+    const float4 a = *reinterpret_cast<const float4*>(yr);
+    const float4 c = *reinterpret_cast<const float4*>(yr + 4);
+    moe[0] += a.x; moe[1] += a.y; moe[2] += a.z; moe[3] += a.w;
+    moe[4] += c.x; moe[5] += c.y; moe[6] += c.z; moe[7] += c.w;
+  }
+  uint4 o;
+  if (!p.full_layer) {
+    o = make_uint4(pack_bf16(moe[0], moe[1]), pack_bf16(moe[2], moe[3]), pack_bf16(moe[4], moe[5]),
+                   pack_bf16(moe[6], moe[7]));
+  } else {
+    float dv[8];
+    {
+      const float* dr = b.d + static_cast<size_t>(t) * H + f;
+      const float4 a = *reinterpret_cast<const float4*>(dr);
+      const float4 c = *reinterpret_cast<const float4*>(dr + 4);
+      dv[0] = a.x; dv[1] = a.y; dv[2] = a.z; dv[3] = a.w;
+      dv[4] = c.x; dv[5] = c.y; dv[6] = c.z; dv[7] = c.w;
+    }
+    float sd = 0.0f, sm = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sd = fmaf(dv[j], dv[j], sd);
+      sm = fmaf(moe[j], moe[j], sm);
+    }
+    sd = block_sum(sd, red);
+    sm = block_sum(sm, red);
+    const float inv_d = 1.0f / sqrtf(sd / static_cast<float>(H) + p.eps);
+    const float inv_m = 1.0f / sqrtf(sm / static_cast<float>(H) + p.eps);
+    float s[8];
+    float ss = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      s[j] = dv[j] * inv_d * (1.0f + p.post_ff_ln_1[f + j]) + moe[j] * inv_m * (1.0f + p.post_ff_ln_2[f + j]);
+      ss = fmaf(s[j], s[j], ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv_s = 1.0f / sqrtf(ss / static_cast<float>(H) + p.eps);
+    const uint4 xv = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + f);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    uint32_t ow[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = (bf16_lo(xw[j]) + s[2 * j] * inv_s * (1.0f + p.post_ff_ln[f + 2 * j])) * p.layer_scalar;
+      const float hi =
+          (bf16_hi(xw[j]) + s[2 * j + 1] * inv_s * (1.0f + p.post_ff_ln[f + 2 * j + 1])) * p.layer_scalar;
+      ow[j] = pack_bf16(lo, hi);
+    }
+    o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  }
+  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H + f) = o;
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const RouteParams& p, const Buffers& b, cudaStream_t s) {
+  dim3 grid((p.T + kRouterTok - 1) / kRouterTok, E / kRouterExp, p.ks);
+  router_logits_kernel<<<grid, 256, 0, s>>>(p, b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s) {
+  const int tb = 8 * p.tpw;
+  route_topk_kernel<<<(p.T + tb - 1) / tb, 256, 0, s>>>(p, b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scatter(const RouteParams& p, const Buffers& b, cudaStream_t s) {
+  route_scatter_kernel<<<(p.T + kScatterTok - 1) / kScatterTok, 256, 0, s>>>(p, b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, const Buffers& b, cudaStream_t s) {
+  combine_kernel<<<p.T, kCombineThreads, 0, s>>>(p, b);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

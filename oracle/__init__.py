@@ -17,7 +17,6 @@ Pins (what the oracle is checked against, in ``tests/test_oracle_pins.py``):
   * The permutation against a brute-force sort of the slots by (expert, token).
 """
 import ctypes
-import os
 
 import numpy as np
 
@@ -94,6 +93,9 @@ def lib():
         L.moe_oracle_forward.restype = ctypes.c_int
         L.moe_oracle_forward.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _u16p,
                                          ctypes.POINTER(Weights), ctypes.POINTER(Outputs), ctypes.c_int]
+        L.moe_oracle_route.restype = ctypes.c_int
+        L.moe_oracle_route.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _u16p, ctypes.POINTER(Weights),
+                                       ctypes.POINTER(Outputs)]
         L.moe_oracle_permute.restype = ctypes.c_int
         L.moe_oracle_permute.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _f32p,
                                          _i32p, _i32p, _i32p, _f32p, _i32p]
@@ -144,7 +146,8 @@ WEIGHT_FIELDS_F32 = ("router_w", "router_norm_w", "per_expert_scale", "pre_ff_ln
 WEIGHT_FIELDS_BF16 = ("gate_up", "down", "dense_gate", "dense_up", "dense_down")
 
 
-def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked_dense=False) -> dict:
+def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked_dense=False,
+            route_only=False) -> dict:
     """Runs the block on host arrays.
 
     dims: hidden, n_experts, top_k, moe_inter, dense_inter, full_layer, eps, router_scale and
@@ -152,6 +155,7 @@ def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked
       arrays, float32 for the fp32 fields and uint16 bf16 bit patterns for the bf16 fields (the
       dense and norm fields may be absent when full_layer is 0), plus the float layer_scalar.
     want: names of the outputs to return (fields of moe_oracle_outputs).
+    route_only: run only the router (moe_oracle_route); only router outputs may be wanted.
     """
     H, E, K = dims["hidden"], dims["n_experts"], dims["top_k"]
     I, D = dims["moe_inter"], dims.get("dense_inter", 0)
@@ -175,7 +179,11 @@ def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked
             keep[f] = a
             setattr(wst, f, _ptr(a, ctypes.c_uint16))
     wst.layer_scalar = float(weights.get("layer_scalar", 1.0))
-    if full:
+    if route_only:
+        missing = [f for f in ("router_w", "router_norm_w", "per_expert_scale") if f not in keep]
+        if full and dims.get("router_reads_pre2", 0) and "pre_ff_ln_2" not in keep:
+            missing.append("pre_ff_ln_2")
+    elif full:
         missing = [f for f in WEIGHT_FIELDS_F32 + WEIGHT_FIELDS_BF16 if f not in keep]
     else:
         missing = [f for f in ("router_w", "router_norm_w", "per_expert_scale", "gate_up", "down") if f not in keep]
@@ -197,8 +205,12 @@ def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked
         res[name] = a
         ctype = {np.float64: ctypes.c_double, np.float32: ctypes.c_float, np.int32: ctypes.c_int32}[dt]
         setattr(ost, name, _ptr(a, ctype))
-    rc = lib().moe_oracle_forward(ctypes.byref(d), T, _ptr(x, ctypes.c_uint16), ctypes.byref(wst),
-                                  ctypes.byref(ost), 1 if masked_dense else 0)
+    if route_only:
+        rc = lib().moe_oracle_route(ctypes.byref(d), T, _ptr(x, ctypes.c_uint16), ctypes.byref(wst),
+                                    ctypes.byref(ost))
+    else:
+        rc = lib().moe_oracle_forward(ctypes.byref(d), T, _ptr(x, ctypes.c_uint16), ctypes.byref(wst),
+                                      ctypes.byref(ost), 1 if masked_dense else 0)
     if rc != 0:
         raise RuntimeError("moe_oracle_forward failed (%d)" % rc)
     return res
@@ -232,4 +244,3 @@ def gemma_dims(full_layer: bool) -> dict:
 
 __all__ = ["lib", "gelu_tanh", "rmsnorm", "forward", "permute", "set_threads", "max_threads",
            "gemma_dims", "Dims", "Weights", "Outputs"]
-_ = os

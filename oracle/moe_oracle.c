@@ -275,6 +275,43 @@ int moe_oracle_forward(const moe_oracle_dims* d, int T, const uint16_t* x,
   return bad ? -1 : 0;
 }
 
+int moe_oracle_route(const moe_oracle_dims* d, int T, const uint16_t* x, const moe_oracle_weights* w,
+                     const moe_oracle_outputs* o) {
+  if (!dims_ok(d) || T < 0 || !w || !o || (T > 0 && !x)) return -1;
+  const int H = d->hidden, E = d->n_experts, K = d->top_k;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+  for (int t = 0; t < T; ++t) {
+    double* xd = malloc(sizeof(double) * H);
+    double* n2 = malloc(sizeof(double) * H);
+    float* xin = malloc(sizeof(float) * H);
+    float* r = malloc(sizeof(float) * H);
+    float* logits = malloc(sizeof(float) * E);
+    float* probs = malloc(sizeof(float) * E);
+    int32_t* idx = malloc(sizeof(int32_t) * K);
+    float* wren = malloc(sizeof(float) * K);
+    float* wfin = malloc(sizeof(float) * K);
+    if (!xd || !n2 || !xin || !r || !logits || !probs || !idx || !wren || !wfin) {
+      bad |= 1;
+    } else {
+      for (int h = 0; h < H; ++h) xd[h] = (double)bf16_to_f32(x[(size_t)t * H + h]);
+      if (d->full_layer && d->router_reads_pre2) moe_oracle_rmsnorm(xd, w->pre_ff_ln_2, H, (double)d->eps, n2);
+      for (int h = 0; h < H; ++h)
+        xin[h] = (d->full_layer && d->router_reads_pre2) ? (float)n2[h] : (float)xd[h];
+      float gap;
+      route_one(d, xin, w, r, logits, probs, idx, wren, wfin, &gap);
+      if (o->logits) memcpy(o->logits + (size_t)t * E, logits, sizeof(float) * E);
+      if (o->probs) memcpy(o->probs + (size_t)t * E, probs, sizeof(float) * E);
+      if (o->topk_idx) memcpy(o->topk_idx + (size_t)t * K, idx, sizeof(int32_t) * K);
+      if (o->topk_w_renorm) memcpy(o->topk_w_renorm + (size_t)t * K, wren, sizeof(float) * K);
+      if (o->topk_w) memcpy(o->topk_w + (size_t)t * K, wfin, sizeof(float) * K);
+      if (o->gap) o->gap[t] = gap;
+    }
+    free(xd); free(n2); free(xin); free(r); free(logits); free(probs); free(idx); free(wren); free(wfin);
+  }
+  return bad ? -1 : 0;
+}
+
 /* Slots sorted by (expert, token): the gather that precedes each expert's MLP and the scatter
  * back ([MoE] "The architecture": the experts' sparse gather/scatter loop), as a counting sort. */
 int moe_oracle_permute(int T, int K, int E, const int32_t* topk_idx, const float* topk_w,

@@ -92,6 +92,12 @@ void moe_oracle_rmsnorm(const double* v, const float* w, int n, double eps, doub
 int moe_oracle_forward(const moe_oracle_dims* d, int T, const uint16_t* x,
                        const moe_oracle_weights* w, const moe_oracle_outputs* o, int masked_dense);
 
+/* Only the router of the block for T tokens: fills the logits, probs, topk_idx, topk_w_renorm,
+ * topk_w and gap fields of *o (the others are ignored), exactly as moe_oracle_forward would.
+ * Returns 0, or -1 on bad arguments. */
+int moe_oracle_route(const moe_oracle_dims* d, int T, const uint16_t* x, const moe_oracle_weights* w,
+                     const moe_oracle_outputs* o);
+
 /* Stable counting sort of the T*K slots by expert: counts[E], offsets[E+1] (exclusive prefix sum,
  * offsets[E] = T*K), perm[T*K] (token of each sorted slot; within one expert tokens ascend),
  * w_sorted[T*K] (topk_w of each sorted slot; may be NULL with topk_w NULL), slot_pos[T*K] (sorted

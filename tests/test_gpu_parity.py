@@ -1,0 +1,139 @@
+"""CUDA path vs the oracle, through the C ABI, on the same seeded inputs (GB300 only).
+
+Shapes: the five workloads of the block (experts-only T=8; full layer T=64; full layer T=4096
+with skewed routing; the sweep's T values incl. the maximum 16384) plus ragged and degenerate
+cases. Where the oracle cannot run every token in seconds, it runs the router on every token
+(expert choice and the permutation are checked in full) and the whole block on a sample.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_router_gb300 import binding as B
+from mixture_experts_ffn_router_gb300 import synth
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+MOE, FULL = B.MOE_FFN_MOE_ONLY, B.MOE_FFN_FULL_LAYER
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.lib()  # fails loudly if the library is missing
+
+
+def _full_check(mode, T, seed, skew=False, label=""):
+    x, w = G.make_case(mode, T, seed, skew=skew)
+    run = G.Run(mode, x, w)
+    wh = G.host_weights(w)
+    xb = synth.bf16_bits(x)
+    ref = G.oracle_forward(mode, xb, wh)
+    same = G.check_routing(run, ref)
+    G.check_permutation(run)
+    frob, mx = G.check_values(run.out_f64[same], ref["out"][same], label)
+    return run, ref, frob, mx
+
+
+@pytest.mark.parametrize("T", [8, 1, 3, 31, 32, 33])
+def test_moe_only_small(T):
+    _full_check(MOE, T, 100 + T, label="moe-only T=%d" % T)
+
+
+@pytest.mark.parametrize("T", [64, 1, 65, 200])
+def test_full_layer(T):
+    _full_check(FULL, T, 200 + T, label="full T=%d" % T)
+
+
+def _sampled_check(mode, T, seed, skew, n_sample, label):
+    x, w = G.make_case(mode, T, seed, skew=skew)
+    run = G.Run(mode, x, w)
+    wh = G.host_weights(w)
+    xb = synth.bf16_bits(x)
+    route = G.oracle_route(mode, xb, wh)
+    same = G.check_routing(run, route)
+    G.check_permutation(run)
+    rng = np.random.default_rng(seed)
+    tok = np.sort(rng.choice(T, size=min(n_sample, T), replace=False))
+    tok = np.unique(np.concatenate([tok, [0, T - 1]]))
+    ref = G.oracle_forward(mode, xb, wh, tokens=tok, want=("out",))
+    keep = same[tok]
+    frob, mx = G.check_values(run.out_f64[tok][keep], ref["out"][keep], label)
+    return run, route
+
+
+def test_full_layer_prefill_skewed_4096():
+    run, route = _sampled_check(FULL, 4096, 300, True, 48, "full T=4096 skewed")
+    load = run.counts
+    assert load.max() >= 6 * load.mean()      # a heavily loaded head ...
+    assert (load == 0).sum() >= 8             # ... and experts with no tokens
+
+
+@pytest.mark.parametrize("T", [256, 1024, 1500])
+def test_full_layer_sweep_sizes(T):
+    _sampled_check(FULL, T, 400 + T, False, 32, "full T=%d" % T)
+
+
+@pytest.mark.slow
+def test_full_layer_max_sweep_16384():
+    _sampled_check(FULL, 16384, 500, False, 24, "full T=16384")
+
+
+def test_all_tokens_identical_pick_the_same_experts():
+    # Identical tokens choose the same 8 experts: 8 experts get all T tokens (several token tiles
+    # each), the other 120 get none.
+    T = 300
+    x1, w = G.make_case(FULL, 1, 600)
+    x = x1.expand(T, -1).contiguous()
+    run = G.Run(FULL, x, w)
+    assert (run.counts > 0).sum() == 8 and run.counts.max() == T
+    G.check_permutation(run)
+    ref = G.oracle_forward(FULL, synth.bf16_bits(x1), G.host_weights(w))
+    if ref["gap"][0] > G.GAP_MIN:
+        np.testing.assert_array_equal(run.topk_idx[0], ref["topk_idx"][0])
+    np.testing.assert_array_equal(run.out_f64, np.broadcast_to(run.out_f64[:1], run.out_f64.shape))
+    G.check_values(run.out_f64[:1], ref["out"], "identical tokens")
+
+
+def test_deterministic_bitwise():
+    x, w = G.make_case(FULL, 500, 700)
+    m = B.MoeFFN(FULL, 500)
+    a = m.forward(x, w).clone()
+    b = m.forward(x, w).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_context_reuse_across_T_and_weights():
+    # One context, calls with different T and different weights: each result equals a fresh run.
+    m = B.MoeFFN(FULL, 256)
+    for T, seed in [(256, 800), (17, 801), (130, 802)]:
+        x, w = G.make_case(FULL, T, seed)
+        a = m.forward(x, w).clone()
+        fresh = B.MoeFFN(FULL, T).forward(x, w)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), fresh.view(torch.int16))
+
+
+def test_error_paths():
+    m = B.MoeFFN(FULL, 16)
+    x, w = G.make_case(FULL, 16, 900)
+    ws = B.weights_struct(w)
+    out = torch.empty_like(x)
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.moe_ffn_forward(m.ctx, x.data_ptr(), 17, ws, out.data_ptr(), s) == B.MOE_FFN_ETOOBIG
+    assert B.moe_ffn_forward(m.ctx, x.data_ptr(), -1, ws, out.data_ptr(), s) == B.MOE_FFN_EINVAL
+    assert B.moe_ffn_forward(m.ctx, x.data_ptr(), 0, ws, out.data_ptr(), s) == B.MOE_FFN_OK
+    assert B.moe_ffn_forward(m.ctx, x.data_ptr() + 2, 4, ws, out.data_ptr(), s) == B.MOE_FFN_EALIGN
+    assert B.moe_ffn_forward(m.ctx, 0, 4, ws, out.data_ptr(), s) == B.MOE_FFN_EINVAL
+    assert B.moe_ffn_forward(m.ctx, x.data_ptr(), 16, ws, x.data_ptr(), s) == B.MOE_FFN_EINVAL  # out aliases x
+    bad = B.weights_struct(w)
+    bad.dense_down = None
+    assert B.moe_ffn_forward(m.ctx, x.data_ptr(), 4, bad, out.data_ptr(), s) == B.MOE_FFN_EINVAL
+    cfg = B.make_config(FULL, 16)
+    cfg.hidden = 4096
+    assert B.moe_ffn_workspace_bytes(cfg) == 0
+    torch.cuda.synchronize()
+    assert m.status() == (B.MOE_FFN_OK, 0)

@@ -270,3 +270,14 @@ def test_permutation_is_the_stable_sort_by_expert(T, E, K, seed):
 def test_permutation_rejects_bad_expert_ids():
     with pytest.raises(ValueError):
         oracle.permute(np.array([[0, 9]], np.int32), None, 8)
+
+
+def test_route_only_matches_forward():
+    x, w = tiny.case(tiny.SMALL, 50, 16, full_layer=True, weight_std=0.3)
+    for pre2 in (False, True):
+        d = tiny.dims_of(tiny.SMALL, full_layer=True, router_reads_pre2=pre2)
+        want = ("logits", "probs", "topk_idx", "topk_w", "topk_w_renorm", "gap")
+        a = oracle.forward(d, x, w, want=want)
+        b = oracle.forward(d, x, w, want=want, route_only=True)
+        for k in want:
+            np.testing.assert_array_equal(a[k], b[k])
