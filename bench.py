@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of the Gemma-4 26B-A4B sparse MoE feed-forward block on GB300.
+
+One step = one forward of the whole block (router, top-k, permutation, gate_up and down grouped
+GEMMs, combine with the post-norms) over one batch of synthetic tokens, through the C ABI.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload decode64|prefill4096|moe8|layer --T T]
+  python bench.py --impl reference ...      (the oracle, timed on the host cores)
+
+Default workload: the full dual-path layer at decode batch T=64, uniform routing. Multi-GPU runs
+(torchrun, one rank per GPU) are weak scaling: each rank runs its own replica of the layer on its
+own 64 tokens; there is no data-path collective. Prints one JSON line (rank 0).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-FFN tokens/s at T=64 & T=4096; % of HBM or bf16 TC roofline"
+UNIT = "tokens/s"
+H, E, K, I, D = 2816, 128, 8, 704, 2112
+
+# Algorithmic bytes per unit: one expert's gate_up and down slices, the shared
+# MLP's matrices, the router matrix.
+GATE_UP_BYTES_PER_EXPERT = 2 * I * H * 2        # 7,929,856
+DOWN_BYTES_PER_EXPERT = H * I * 2               # 3,964,928
+DENSE_GATE_UP_BYTES = 2 * D * H * 2             # 23,789,568
+DENSE_DOWN_BYTES = H * D * 2                    # 11,894,784
+ROUTER_BYTES = E * H * 4                        # 1,441,792
+FLOPS_PER_TOKEN_EXPERTS = K * 2 * (2 * I * H + H * I)   # 95,158,272
+FLOPS_PER_TOKEN_DENSE = 2 * (2 * D * H + H * D)         # 35,684,352
+
+WORKLOADS = {
+    "decode64": dict(full=True, T=64, skew=False,
+                     desc="Gemma-4 26B-A4B full dual-path FFN layer, decode batch T=64, uniform routing"),
+    "prefill4096": dict(full=True, T=4096, skew=True,
+                        desc="Gemma-4 26B-A4B full dual-path FFN layer, prefill T=4096, Zipf(1.1)-scaled router rows"),
+    "moe8": dict(full=False, T=8, skew=False, desc="Gemma-4 26B-A4B MoE block only (router + experts), T=8"),
+    "layer": dict(full=True, T=None, skew=False, desc="Gemma-4 26B-A4B full dual-path FFN layer, uniform routing"),
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode64")
+    p.add_argument("--T", type=int, default=None, help="tokens per step for --workload layer")
+    p.add_argument("--seed", type=int, default=1234)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def workload_of(args):
+    w = dict(WORKLOADS[args.workload])
+    if w["T"] is None:
+        if not args.T:
+            raise SystemExit("--workload layer needs --T")
+        w["T"] = args.T
+        w["desc"] = w["desc"] + ", T=%d" % args.T
+    return w
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def job_throughput(tokens_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * steps * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None, period_ms=100):
+        self.uuid = uuid
+        self.period_ms = period_ms
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+        return self
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if len(r) >= 10 and (self.uuid is None or self.uuid in r[1])]
+        timed = [r for (t, r) in self.rows if t0 <= t <= t1 and len(r) >= 10 and (self.uuid is None or self.uuid in r[1])]
+        use = timed or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in use if num(r[2]) is not None]
+        mx = [num(r[3]) for r in use if num(r[3]) is not None]
+        reasons = set()
+        names = {6: "hw_slowdown", 7: "hw_thermal_slowdown", 8: "sw_thermal_slowdown", 9: "sw_power_cap"}
+        for r in use:
+            for i, n in names.items():
+                if r[i].lower().startswith("active"):
+                    reasons.add(n)
+        pw = [num(r[4]) for r in use if num(r[4]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(timed),
+                "power_w_max": max(pw) if pw else None}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get("%s/%s" % (kernel, workload))
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec.get("dram_bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
+
+
+# ------------------------------------------------------------------ the CPU arms (oracle)
+
+def oracle_tokens_per_s(wl, w_host, x_bits, n_tokens, repeats=3):
+    """Times the oracle on the host cores over the first n_tokens of one step's batch (host copies
+    of the tensors the GPU arm used)."""
+    import oracle
+    x = x_bits[:n_tokens]
+    w = w_host
+    dims = oracle.gemma_dims(wl["full"])
+    best = None
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.forward(dims, x, w, want=("out",))
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    return n_tokens / best, oracle.max_threads(), best
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from mixture_experts_ffn_router_gb300 import synth
+    T = wl["T"]
+    n = min(T, 64)
+    w = synth.host_arrays(synth.make_weights(seed=args.seed, device="cpu", full_layer=wl["full"], skew=wl["skew"]))
+    x = synth.bf16_bits(synth.make_x(T, seed=args.seed, device="cpu"))[:n]
+    dims = oracle.gemma_dims(wl["full"])
+    for _ in range(max(args.warmup, 0)):
+        oracle.forward(dims, x, w, want=("out",))
+    steps = max(1, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.forward(dims, x, w, want=("out",))
+    dt = time.perf_counter() - t0
+    value = n * steps / dt
+    sample = "first %d of the %d tokens of one step, %d steps" % (n, T, steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (router f32)", "data": "synthetic",
+        "config": {"workload": wl["desc"], "T": T},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def run_ours(args, wl):
+    import numpy as np
+    import torch
+    from mixture_experts_ffn_router_gb300 import binding as B
+    from mixture_experts_ffn_router_gb300 import synth
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T = wl["T"]
+    mode = B.MOE_FFN_FULL_LAYER if wl["full"] else B.MOE_FFN_MOE_ONLY
+
+    w = synth.make_weights(seed=args.seed, device=dev, full_layer=wl["full"], skew=wl["skew"])
+    x = synth.make_x(T, seed=args.seed, device=dev)
+    out = torch.empty_like(x)
+    m = B.MoeFFN(mode, T, device=local)
+    ws = B.weights_struct(w)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+
+    def step():
+        rc = B.moe_ffn_forward(m.ctx, x.data_ptr(), T, ws, out.data_ptr(), s)
+        if rc != B.MOE_FFN_OK:
+            raise B.MoeFFNError("moe_ffn_forward", rc)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    rc, word = m.status()
+    if rc != B.MOE_FFN_OK:
+        raise RuntimeError("device status 0x%x after warm-up" % word)
+    v = m.views()
+    counts = B.view_tensor(v.counts, (E,), torch.int32).cpu().numpy()
+    experts_hit = int((counts > 0).sum())
+
+    # Per-step, per-kernel events (recorded by the library around each of its launches).
+    nk = B.moe_ffn_kernels_per_forward(m.ctx, T)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
+          for _ in range(args.steps)]
+    for row in ev:
+        for a, b in row:
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid=uuid).start()
+    time.sleep(0.3)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        for k in range(nk):
+            B.moe_ffn_set_kernel_events(m.ctx, k, ev[i][k][0].cuda_event, ev[i][k][1].cuda_event)
+        step()
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world, dev)
+    for k in range(nk):
+        B.moe_ffn_set_kernel_events(m.ctx, k, None, None)
+    time.sleep(0.25)
+    clocks.stop()
+    rc, word = m.status()
+    if rc != B.MOE_FFN_OK:
+        raise RuntimeError("device status 0x%x after the timed steps" % word)
+
+    ms = t_start.elapsed_time(t_stop)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = job_throughput(T, args.steps, world, ms_max / 1e3)
+    kernel_us = {B.KERNEL_NAMES[k]: float(np.mean([ev[i][k][0].elapsed_time(ev[i][k][1]) for i in range(args.steps)]) * 1e3)
+                 for k in range(nk)}
+
+    # ---- roofline of the dominant kernel and of the whole layer
+    hbm, tc_burst, tc_sus, peak_src = measured_peaks()
+    S = T * K
+    full = wl["full"]
+    gu_bytes = experts_hit * GATE_UP_BYTES_PER_EXPERT + (DENSE_GATE_UP_BYTES if full else 0) \
+        + T * H * 2 * (2 if full else 1) + S * I * 2 + (T * D * 2 if full else 0)
+    gu_flops = 2 * S * 2 * I * H + (2 * T * 2 * D * H if full else 0)
+    dn_bytes = experts_hit * DOWN_BYTES_PER_EXPERT + (DENSE_DOWN_BYTES if full else 0) \
+        + S * I * 2 + (T * D * 2 if full else 0) + S * H * 4 + (T * H * 4 if full else 0)
+    dn_flops = 2 * S * H * I + (2 * T * H * D if full else 0)
+    per_kernel = {"gate_up_gemm": (gu_bytes, gu_flops), "down_gemm": (dn_bytes, dn_flops)}
+    dom = max(kernel_us, key=kernel_us.get)
+    if dom not in per_kernel:
+        dom = "gate_up_gemm"
+    kb, kf = per_kernel[dom]
+    dur_s = kernel_us[dom] / 1e6
+    if kb / (hbm * 1e9) >= kf / (tc_burst * 1e12):
+        roof = {"bound": "hbm", "achieved": kb / dur_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": kf / dur_s / 1e12, "peak": tc_burst, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_record(dom, args.workload if args.workload != "layer" else "layer_T%d" % T)
+    roof["kernel"] = dom
+    roof["algorithmic_bytes"] = kb
+    roof["algorithmic_flops"] = kf
+    roof["peak_source"] = peak_src
+    layer_bytes = experts_hit * (GATE_UP_BYTES_PER_EXPERT + DOWN_BYTES_PER_EXPERT) + ROUTER_BYTES + T * H * 2 * 2 \
+        + ((DENSE_GATE_UP_BYTES + DENSE_DOWN_BYTES) if full else 0)
+    layer_flops = T * (FLOPS_PER_TOKEN_EXPERTS + (FLOPS_PER_TOKEN_DENSE if full else 0))
+    t_roof = max(layer_bytes / (hbm * 1e9), layer_flops / (tc_burst * 1e12))
+    step_s = ms / args.steps / 1e3
+    layer = {"bytes": layer_bytes, "flops": layer_flops, "roofline_us": t_roof * 1e6, "step_us": step_s * 1e6,
+             "frac": t_roof / step_s, "bound": "hbm" if layer_bytes / (hbm * 1e9) >= layer_flops / (tc_burst * 1e12) else "tensor",
+             "experts_hit": experts_hit}
+
+    # ---- end to end through the public API with host buffers
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    e_steps = max(1, min(args.steps, 500))
+    x_dev = torch.empty_like(x)
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        rc = B.moe_ffn_forward(m.ctx, x_dev.data_ptr(), T, ws, out.data_ptr(), s)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    e0.record(stream)
+    for _ in range(e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        rc = B.moe_ffn_forward(m.ctx, x_dev.data_ptr(), T, ws, out.data_ptr(), s)
+        if rc != B.MOE_FFN_OK:
+            raise B.MoeFFNError("moe_ffn_forward", rc)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": job_throughput(T, e_steps, world, e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2, "steps": e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(T, 64)
+        tps, cores, secs = oracle_tokens_per_s(wl, synth.host_arrays(w), synth.bf16_bits(x), n)
+        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "first %d tokens of the step's batch, best of 3 (%.2f s each)" % (n, secs)}
+
+    clk = clocks.summary(wall0, wall1)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl["desc"], "T": T, "tokens_per_gpu": T, "hidden": H, "experts": E, "top_k": K,
+                       "moe_inter": I, "dense_inter": D if wl["full"] else 0,
+                       "l2": "inputs larger than L2 (%.2f GB of weights read per step)" % (layer_bytes / 1e9),
+                       "parallelism": "replicas (dp%d, no collective)" % world},
+            "roofline": roof, "layer_roofline": layer, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": nk * args.steps, "clocks": clk, "kernels_us": kernel_us,
+        }
+        print(json.dumps(line), flush=True)
+    m.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    wl = workload_of(args)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
