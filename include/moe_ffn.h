@@ -113,7 +113,7 @@ typedef struct moe_ffn_views {
   const uint16_t* n2;         /* [T, 2816] bf16 expert input: pre_feedforward_layernorm_2(x), or x */
   const uint16_t* h;          /* [S, 704] bf16 gelu_tanh(gate) * up per sorted slot */
   const uint16_t* h_dense;    /* [T, 2112] bf16 shared-MLP activation (FULL_LAYER) */
-  const float* y;             /* [S, 2816] fp32 weighted expert output per sorted slot */
+  const uint16_t* y;          /* [S, 2816] bf16 weighted expert output per sorted slot */
   const float* d;             /* [T, 2816] fp32 shared-MLP output (FULL_LAYER) */
   int T;                      /* tokens of that forward */
 } moe_ffn_views;
@@ -153,8 +153,8 @@ int moe_ffn_device_status(moe_ffn_ctx* ctx, void* stream, uint32_t* word);
 
 /* Profiling hook: from now on every forward records `start` (a cudaEvent_t as void*) on its stream
  * right before the launch of kernel `kernel` and `stop` right after it. NULL events turn the hook
- * off. kernel: 0 router logits, 1 top-k and pre-norms, 2 permutation, 3 gate_up grouped GEMM,
- * 4 down grouped GEMM, 5 combine and post-norms. */
+ * off. kernel: 0 router matrix split, 1 router logits, 2 top-k and pre-norms, 3 permutation,
+ * 4 gate_up grouped GEMM, 5 down grouped GEMM, 6 combine and post-norms. */
 int moe_ffn_set_kernel_events(moe_ffn_ctx* ctx, int kernel, void* start, void* stop);
 
 /* Number of kernels one forward of T tokens launches on the device (0 for T = 0). */

@@ -21,7 +21,7 @@ MOE_FFN_EDEVICE = -6
 MOE_FFN_MOE_ONLY = 0
 MOE_FFN_FULL_LAYER = 1
 HIDDEN, N_EXPERTS, TOP_K, MOE_INTER, DENSE_INTER = 2816, 128, 8, 704, 2112
-KERNEL_NAMES = ("router_logits", "route_topk", "route_scatter", "gate_up_gemm", "down_gemm", "combine")
+KERNEL_NAMES = ("router_prep", "router_logits", "route_topk", "route_scatter", "gate_up_gemm", "down_gemm", "combine")
 
 _vp = ctypes.c_void_p
 

@@ -12,17 +12,25 @@
 // weight tile exactly once at full tile height. Work items are (token tile, 128-row weight tile)
 // pairs; the token tiles of the experts come from a device-side list built by the top-k kernel,
 // the shared MLP is one more group over all T tokens. Each CTA is persistent and takes every
-// gridDim-th item, so the result does not depend on timing: every output element is written by
-// exactly one CTA, with a fixed K order.
+// gridDim-th item; every output element is written by exactly one CTA with a fixed K order, so
+// results are bitwise reproducible.
 //
-// Warp roles (192 threads): warp 0 loads A (weights, 2-D TMA boxes) and B (token rows, TMA
-// gather4 by row index) into a ring of shared-memory stages; warp 1 issues tcgen05.mma into one of
-// two TMEM accumulators; warps 2..5 drain the other accumulator (tcgen05.ld) and run the epilogue.
+// Operand loading. A (weights): 2-D TMA boxes of 64 K-elements (one 128-byte swizzled row) by 64
+// (gate_up: gate rows, then up rows) or 128 (down) rows. B (tokens): when the token rows are
+// contiguous in memory (the shared MLP's n1 / h_dense, the experts' h in sorted-slot order) one
+// 2-D TMA box of BN rows; for the experts' gate_up input the rows are gathered by token index from
+// n2 with cp.async by four gather warps, which write the same 128-byte-swizzled layout TMA would.
+// A stage holds KC consecutive K chunks of 64 (KC = 2 for narrow token tiles, so each weight row is
+// fetched 256 bytes at a time).
 //
-// gate_up epilogue: the A tile holds, per 32-row TMEM quarter, 16 gate rows then the 16 up rows of
-// the same features, so one warp sees gate and up of a feature in lanes l and l+16 and forms
-// h = gelu_tanh(gate) * up with one shuffle; h is stored bf16 in sorted-slot order.
-// down epilogue: y[slot] = w_slot * acc (fp32, sorted-slot order); the shared MLP writes d.
+// Warp roles: warp 0 TMA producer; warp 1 MMA issuer (one thread); warps 2..5 epilogue, warp w
+// reading TMEM lanes 32*(w%4).. ; gate_up only: warps 6..9 gather. Two TMEM accumulators let the
+// epilogue of one item overlap the main loop of the next.
+//
+// gate_up epilogue: TMEM lanes 0..63 hold gate, 64..127 up, of features f0..f0+63. The warps of
+// quarters q and q+2 hold gate and up of the same 32 features; each hands half of its columns to
+// the other through shared memory, and each then forms h = gelu_tanh(gate) * up for 16 columns.
+// down epilogue: y[slot] = w_slot * acc (bf16, sorted-slot order); the shared MLP writes d (fp32).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -33,27 +41,34 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;                 // bf16 elements per 128-byte swizzled row
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kThreads = 192;
-constexpr int kSmemBudget = 196608;
+constexpr int kBK = 64;                    // bf16 elements per 128-byte swizzled row
+constexpr int kAChunk = kBM * kBK * 2;     // 16 KB of A per K chunk
+constexpr int kStageBudget = 204800;       // shared memory for the stage ring
 
 template <int BN, bool GATE_UP>
 struct Cfg {
-  static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 10 ? 10 : kStagesRaw;
+  static constexpr int KC = BN <= 64 ? 2 : 1;
+  static constexpr int kBChunk = BN * kBK * 2;
+  static constexpr int kChunkBytes = kAChunk + kBChunk;
+  static constexpr int kStageBytes = KC * kChunkBytes;
+  static constexpr int kStagesRaw = kStageBudget / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kGatherWarps = GATE_UP ? 4 : 0;
+  static constexpr int kThreads = (6 + kGatherWarps) * 32;
+  static constexpr int kFullArrivals = 1 + kGatherWarps * 32;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int kMtExp = GATE_UP ? I / 64 : H / kBM;       // 11 | 22 weight tiles per expert
-  static constexpr int kMtDense = GATE_UP ? D / 64 : H / kBM;     // 33 | 22
-  static constexpr int kKbExp = GATE_UP ? H / kBK : I / kBK;      // 44 | 11
-  static constexpr int kKbDense = GATE_UP ? H / kBK : D / kBK;    // 44 | 33
+  static constexpr int kMtExp = GATE_UP ? I / 64 : H / kBM;        // 11 | 22 weight tiles per expert
+  static constexpr int kMtDense = GATE_UP ? D / 64 : H / kBM;      // 33 | 22
+  static constexpr int kChunksExp = GATE_UP ? H / kBK : I / kBK;   // 44 | 11 K chunks
+  static constexpr int kChunksDense = GATE_UP ? H / kBK : D / kBK; // 44 | 33
+  // gate_up: the gate/up hand-over [4 warps][16][32] fp32; down: a 32x32 output chunk per warp.
+  static constexpr int kXchgBytes = GATE_UP ? 4 * 16 * 32 * 4 : 4 * 32 * 32 * 4;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + BN * 4;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kXchgBytes + kBarBytes;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
-  static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
+  static_assert(kChunkBytes % 1024 == 0, "operand tiles must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(kStages >= 2, "stages");
 };
 
 struct Item {
@@ -90,8 +105,30 @@ __device__ __forceinline__ Item decode_item(int i, int n_dense_items, const int4
   return it;
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Lane 0 waits, the result is broadcast, so the warp stays converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* status, uint32_t why) {
+  int got = 1;
+  if ((threadIdx.x & 31) == 0) got = mbar_wait_bounded(bar, parity, abort_flag, status, why);
+  return __shfl_sync(0xffffffffu, got, 0) != 0;
+}
+
 template <int BN, bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a_exp, const __grid_constant__ CUtensorMap map_a_d0,
                         const __grid_constant__ CUtensorMap map_a_d1, const __grid_constant__ CUtensorMap map_b_exp,
                         const __grid_constant__ CUtensorMap map_b_dense, Buffers b, int T, int full_layer) {
@@ -99,20 +136,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);  // [4][16][32]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kXchgBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
   uint64_t* accf_bar = empty_bar + C::kStages;  // [2] accumulator ready
   uint64_t* acce_bar = accf_bar + 2;            // [2] accumulator drained
   uint64_t* final_bar = acce_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* idx_s = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], C::kFullArrivals);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -123,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&map_a_exp);
-    prefetch_tmap(&map_b_exp);
+    if (!GATE_UP) prefetch_tmap(&map_b_exp);
     if (full_layer) {
       prefetch_tmap(&map_a_d0);
       if (GATE_UP) prefetch_tmap(&map_a_d1);
@@ -147,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = n_dense_items + n_tiles * C::kMtExp;
 
   if (warp == 0) {
-    // ---------------- producer: TMA loads into the stage ring
+    // ---------------- producer: TMA loads of A, and of B when its rows are contiguous
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     int stage = 0;
@@ -156,63 +193,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
       const Item it = decode_item<BN, GATE_UP>(i, n_dense_items, b.exp_tiles, T);
-      // Source rows of the B operand for the token columns of this tile.
-      for (int j = lane; j < BN; j += 32) {
-        const int jj = min(j, it.rows - 1);
-        int r;
-        if (GATE_UP)
-          r = it.dense ? it.row0 + jj : b.perm[it.row0 + jj];
-        else
-          r = it.row0 + jj;
-        const int lim = GATE_UP ? T : (it.dense ? T : T * K);
-        if (r < 0 || r >= lim) {
-          atomicOr(b.status, kStatusBadIndex);
-          r = 0;
-        }
-        idx_s[j] = r;
-      }
-      __syncwarp();
-      const int n_g4 = (it.rows + 3) >> 2;  // only the valid rows are loaded
-      const uint32_t tx_bytes = kABytes + n_g4 * 512;
-      const int nkb = it.dense ? C::kKbDense : C::kKbExp;
-      for (int kb = 0; kb < nkb; ++kb) {
-        int got = 1;
-        if (lane == 0) got = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
+      const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
+      const bool b_tma = !GATE_UP || it.dense;
+      for (int c0 = 0; c0 < nch; c0 += C::KC) {
+        if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          uint8_t* a_dst = stages + stage * C::kStageBytes;
-          uint8_t* b_dst = a_dst + kABytes;
+          const int nck = min(C::KC, nch - c0);
+          uint8_t* st = stages + stage * C::kStageBytes;
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          mbar_arrive_expect_tx(&full_bar[stage], tx_bytes);
-          const int k0 = kb * kBK;
-          if (GATE_UP) {
-            const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
-            const CUtensorMap* mu = it.dense ? &map_a_d1 : &map_a_exp;
-            const int gbase = it.dense ? it.m * 64 : it.e * (2 * I) + it.m * 64;
-            const int ubase = it.dense ? it.m * 64 : it.e * (2 * I) + I + it.m * 64;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              tma_load_2d(a_dst + (2 * q) * 2048, mg, &full_bar[stage], k0, gbase + 16 * q, pol_w);
-              tma_load_2d(a_dst + (2 * q + 1) * 2048, mu, &full_bar[stage], k0, ubase + 16 * q, pol_w);
+          mbar_arrive_expect_tx(&full_bar[stage], nck * (kAChunk + (b_tma ? C::kBChunk : 0)));
+          for (int cc = 0; cc < nck; ++cc) {
+            uint8_t* a_dst = st + cc * C::kChunkBytes;
+            const int k0 = (c0 + cc) * kBK;
+            if (GATE_UP) {
+              const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
+              const CUtensorMap* mu = it.dense ? &map_a_d1 : &map_a_exp;
+              const int grow = it.dense ? it.m * 64 : it.e * (2 * I) + it.m * 64;
+              const int urow = it.dense ? it.m * 64 : it.e * (2 * I) + I + it.m * 64;
+              tma_load_2d(a_dst, mg, &full_bar[stage], k0, grow, pol_w);
+              tma_load_2d(a_dst + kAChunk / 2, mu, &full_bar[stage], k0, urow, pol_w);
+            } else {
+              const CUtensorMap* ma = it.dense ? &map_a_d0 : &map_a_exp;
+              const int arow = it.dense ? it.m * kBM : it.e * H + it.m * kBM;
+              tma_load_2d(a_dst, ma, &full_bar[stage], k0, arow, pol_w);
             }
-          } else {
-            const CUtensorMap* ma = it.dense ? &map_a_d0 : &map_a_exp;
-            const int arow = it.dense ? it.m * kBM : it.e * H + it.m * kBM;
-            tma_load_2d(a_dst, ma, &full_bar[stage], k0, arow, pol_w);
-          }
-          const CUtensorMap* mb = it.dense ? &map_b_dense : &map_b_exp;
-          for (int g = 0; g < n_g4; ++g) {
-            const int jj = 4 * g;
-            const int r0 = idx_s[jj];
-            const int r1 = idx_s[min(jj + 1, it.rows - 1)];
-            const int r2 = idx_s[min(jj + 2, it.rows - 1)];
-            const int r3 = idx_s[min(jj + 3, it.rows - 1)];
-            tma_gather4(b_dst + g * 512, mb, &full_bar[stage], k0, r0, r1, r2, r3, pol_x);
+            if (b_tma) {
+              const CUtensorMap* mb = it.dense ? &map_b_dense : &map_b_exp;
+              tma_load_2d(a_dst + kAChunk, mb, &full_bar[stage], k0, it.row0, pol_x);
+            }
           }
         }
         __syncwarp();
@@ -221,7 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           phase ^= 1u;
         }
       }
-      __syncwarp();
     }
     // Before the CTA can exit, every TMA load this warp issued must have landed.
     if (lane == 0)
@@ -237,22 +248,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-        const int nkb = (i < n_dense_items) ? C::kKbDense : C::kKbExp;
+        const int nch = (i < n_dense_items) ? C::kChunksDense : C::kChunksExp;
         if (!mbar_wait_bounded(&acce_bar[acc], acc_phase ^ 1u, abort_flag, b.status, kStatusWaitAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int c0 = 0; c0 < nch; c0 += C::KC) {
           if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, b.status, kStatusWaitFull)) {
             ok = false;
             break;
           }
+          // The gathered B rows were written by cp.async (generic proxy); the MMA reads them through
+          // the async proxy.
+          if (GATE_UP) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + stage * C::kStageBytes);
-          const uint64_t a_desc = smem_desc_sw128(a_addr);
-          const uint64_t b_desc = smem_desc_sw128(a_addr + kABytes);
+          const int nck = min(C::KC, nch - c0);
+          const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
+          for (int cc = 0; cc < nck; ++cc) {
+            const uint64_t a_desc = smem_desc_sw128(st + cc * C::kChunkBytes);
+            const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + kAChunk);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::kIdesc, (c0 | cc | k) != 0 ? 1u : 0u);
+          }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
             stage = 0;
@@ -269,17 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_timeout(final_bar, 0, kSpinLimitNs);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ---------------- epilogue warps 2..5; TMEM lane quarter = warp % 4
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
       const Item it = decode_item<BN, GATE_UP>(i, n_dense_items, b.exp_tiles, T);
-      int got = 1;
-      if (lane == 0) got = mbar_wait_bounded(&accf_bar[acc], acc_phase, abort_flag, b.status, kStatusWaitAccFull);
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) break;
+      if (!warp_wait(&accf_bar[acc], acc_phase, abort_flag, b.status, kStatusWaitAccFull)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -288,37 +302,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
         tmem_ld32(t_row + c * 32, v);
         if (GATE_UP) {
-          // lanes 0..15: gate of feature f, lanes 16..31: up of the same feature
-          const int f = it.m * 64 + 16 * q + (lane & 15);
-          const bool is_gate = lane < 16;
+          // q 0/1: gate of features f0+32(q&1)+lane; q 2/3: up of the same features.
+          const bool gate_holder = q < 2;
+          const int pairbar = 1 + (q & 1);
+          float* mine = xchg + q * 512;
+          const float* theirs = xchg + (q ^ 2) * 512;
+          // The gate holder hands over columns 16..31 and finishes 0..15; the up holder the reverse.
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = gate_holder ? v[16 + j] : v[j];
+          named_bar_sync(pairbar, 64);
+          const int f = it.m * 64 + 32 * (q & 1) + lane;
           uint16_t* dst = it.dense ? b.h_dense : b.h;
           const int ld = it.dense ? D : I;
+          const int keep = gate_holder ? 0 : 16;
 #pragma unroll
-          for (int pr = 0; pr < 16; ++pr) {
-            const float send = is_gate ? v[2 * pr + 1] : v[2 * pr];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = is_gate ? v[2 * pr] : recv;
-            const float u = is_gate ? recv : v[2 * pr + 1];
-            const int col = c * 32 + 2 * pr + (is_gate ? 0 : 1);
+          for (int j = 0; j < 16; ++j) {
+            const float other = theirs[j * 32 + lane];
+            const float own = gate_holder ? v[j] : v[16 + j];
+            const float g = gate_holder ? own : other;
+            const float u = gate_holder ? other : own;
+            const int col = c * 32 + keep + j;
             if (col < it.rows) dst[static_cast<size_t>(it.row0 + col) * ld + f] = f32_to_bf16_rn(gelu_tanh_approx(g) * u);
           }
+          named_bar_sync(pairbar, 64);
         } else {
-          const int f = it.m * kBM + 32 * q + lane;
+          // The warp's 32 features x 32 token columns go through shared memory so that the global
+          // stores are 16-byte vectors along the feature dimension.
+          const int f0 = it.m * kBM + 32 * q;
+          uint8_t* stg = reinterpret_cast<uint8_t*>(xchg) + q * 4096;
           if (it.dense) {
+            float* sd = reinterpret_cast<float*>(stg);  // [32 tokens][32 features]
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c * 32 + j;
-              if (col < it.rows) b.d[static_cast<size_t>(it.row0 + col) * H + f] = v[j];
+            for (int j = 0; j < 32; ++j) sd[j * 32 + lane] = v[j];
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int idx = lane + 32 * i, r = idx >> 3, c4 = idx & 7;
+              const int col = c * 32 + r;
+              if (col < it.rows)
+                *reinterpret_cast<float4*>(b.d + static_cast<size_t>(it.row0 + col) * H + f0 + 4 * c4) =
+                    *reinterpret_cast<const float4*>(sd + r * 32 + 4 * c4);
             }
+            __syncwarp();
           } else {
+            // The router weights of this chunk's 32 slots: one coalesced load, then broadcast.
+            const int my_col = c * 32 + lane;
+            const float w_mine = my_col < it.rows ? __ldg(b.w_sorted + it.row0 + my_col) : 0.0f;
+            uint16_t* sy = reinterpret_cast<uint16_t*>(stg);  // [32 slots][32 features] bf16
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c * 32 + j;
-              if (col < it.rows) {
-                const int pos = it.row0 + col;
-                b.y[static_cast<size_t>(pos) * H + f] = v[j] * b.w_sorted[pos];
-              }
+            for (int j = 0; j < 32; ++j) sy[j * 32 + lane] = f32_to_bf16_rn(v[j] * __shfl_sync(0xffffffffu, w_mine, j));
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int idx = lane + 32 * i, r = idx >> 2, c8 = idx & 3;
+              const int col = c * 32 + r;
+              if (col < it.rows)
+                *reinterpret_cast<uint4*>(b.y + static_cast<size_t>(it.row0 + col) * H + f0 + 8 * c8) =
+                    *reinterpret_cast<const uint4*>(sy + r * 32 + 8 * c8);
             }
+            __syncwarp();
           }
         }
       }
@@ -328,6 +370,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+  } else {
+    // ---------------- gather warps 6..9 (gate_up only): expert token rows of n2 by cp.async
+    const int g = threadIdx.x - 192;         // 0..127
+    const int chunk16 = g & 7;               // which 16 bytes of the 128-byte row
+    const int rbase = g >> 3;                // rows rbase, rbase+16, ...
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+      const Item it = decode_item<BN, GATE_UP>(i, n_dense_items, b.exp_tiles, T);
+      const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
+      int src[BN / 16];
+#pragma unroll
+      for (int r = 0; r < BN / 16; ++r) {
+        const int j = rbase + 16 * r;
+        int t = -1;
+        if (!it.dense && j < it.rows) {
+          t = b.perm[it.row0 + j];
+          if (t < 0 || t >= T) {
+            atomicOr(b.status, kStatusBadIndex);
+            t = 0;
+          }
+        }
+        src[r] = t;
+      }
+      for (int c0 = 0; c0 < nch; c0 += C::KC) {
+        if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
+          ok = false;
+          break;
+        }
+        if (!it.dense) {
+          const int nck = min(C::KC, nch - c0);
+          const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
+          for (int cc = 0; cc < nck; ++cc) {
+            const uint32_t b_dst = st + cc * C::kChunkBytes + kAChunk;
+            const int k0 = (c0 + cc) * kBK;
+#pragma unroll
+            for (int r = 0; r < BN / 16; ++r) {
+              const int j = rbase + 16 * r;
+              if (src[r] >= 0) {
+                const uint16_t* s = b.n2 + static_cast<size_t>(src[r]) * H + k0 + chunk16 * 8;
+                cp_async16(b_dst + j * 128 + ((chunk16 ^ (j & 7)) << 4), s);
+              }
+            }
+          }
+        }
+        cp_async_arrive_noinc(&full_bar[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_all();
   }
 
   tc_fence_before();
@@ -342,9 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, bool GATE_UP>
 cudaError_t launch_t(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s) {
   using C = Cfg<BN, GATE_UP>;
-  grouped_gemm_kernel<BN, GATE_UP><<<grid, kThreads, C::kSmem, s>>>(m.a_exp, m.a_dense0, m.a_dense1, m.b_exp,
-                                                                    m.b_dense, b, T, full_layer);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
+                    m.a_dense0, m.a_dense1, m.b_exp, m.b_dense, b, T, full_layer);
 }
 
 template <int BN, bool GATE_UP>

@@ -13,10 +13,8 @@ constexpr int K = 8;      // experts per token
 constexpr int I = 704;    // expert intermediate width
 constexpr int D = 2112;   // shared-MLP intermediate width
 
-// Router-logit kernel tiling: 32 tokens x 64 experts per CTA, K split into `ks` equal parts.
-constexpr int kRouterTok = 32;
-constexpr int kRouterExp = 64;
-constexpr int kRouterKc = 64;
+// Router kernel: 64 tokens per CTA (the MMA's N), the hidden dimension split into `ks` parts.
+constexpr int kRouterN = 64;
 // Token-scatter kernel: 256 tokens per CTA (8 warps of 32).
 constexpr int kScatterTok = 256;
 // Combine kernel: one CTA per token, 352 threads x 8 features.
@@ -29,8 +27,8 @@ struct Buffers {
   int32_t* topk_idx;    // [Tm, 8]
   float* topk_w;        // [Tm, 8]
   float* gap;           // [Tm]
-  int32_t* hist;        // [kMaxRouteBlocks, 128] per-CTA expert counts of the top-k kernel
-  int32_t* base;        // [kMaxRouteBlocks, 128] first sorted position of each (CTA, expert)
+  int32_t* hist;        // [kMaxRouteBlocks, 128] expert counts per 256-token chunk
+  int32_t* base;        // [kMaxRouteBlocks, 128] first sorted position of each (chunk, expert)
   int32_t* counts;      // [128]
   int32_t* offsets;     // [129]
   int32_t* n_exp_tiles; // [1]
@@ -43,13 +41,14 @@ struct Buffers {
   uint16_t* n2;         // [Tm, 2816]
   uint16_t* h;          // [S, 704]
   uint16_t* h_dense;    // [Tm, 2112]
-  float* y;             // [S, 2816]
+  uint16_t* y;          // [S, 2816] bf16
   float* d;             // [Tm, 2816]
   unsigned int* status; // [1]
+  uint16_t* wsplit;     // [3, 128, 2816] bf16: W_r * (1 + router_norm_w) as hi + mid + lo
   int max_tiles;
 };
 
-constexpr int kMaxRouteBlocks = 256;
+constexpr int kMaxRouteBlocks = 256;  // 256-token chunks: 65536 tokens at most
 
 struct RouteParams {
   const uint16_t* x;
@@ -80,13 +79,34 @@ struct CombineParams {
 };
 
 // Maps of one grouped GEMM launch. For gate_up: a_exp = gate_up rows, a_dense0/1 = dense gate/up,
-// b_exp = n2 (gather), b_dense = n1 (gather). For down: a_exp = down rows, a_dense0 = dense down,
-// b_exp = h (gather), b_dense = h_dense (gather).
+// b_dense = n1 (BN-row boxes; the experts' rows are gathered with cp.async, b_exp is unused). For
+// down: a_exp = down rows, a_dense0 = dense down, b_exp = h, b_dense = h_dense (BN-row boxes).
 struct GemmMaps {
   CUtensorMap a_exp, a_dense0, a_dense1, b_exp, b_dense;
 };
 
-cudaError_t launch_router_logits(const RouteParams& p, const Buffers& b, cudaStream_t s);
+// Launches a kernel with programmatic dependent launch: its CTAs may start while the previous
+// kernel on the stream finishes; every kernel here calls griddepcontrol.wait before it touches
+// memory the previous kernels write or read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+constexpr int kKernelsPerForward = 7;
+cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_route_scatter(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, const Buffers& b, cudaStream_t s);
@@ -97,5 +117,6 @@ cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, i
 cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                         cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
+cudaError_t router_set_smem_limit();
 
 }  // namespace moe

@@ -1,22 +1,24 @@
 // moe_ffn.cu — host side of the library: the C ABI of include/moe_ffn.h, workspace layout,
 // TMA tensor maps and the launch sequence of one forward.
 //
-// One forward of T tokens queues six kernels on the caller's stream, in this order:
-//   0 router logits   fp32 partial projections of the router ("The architecture": own RMSNorm,
-//                     a scale, softmax over 128 experts in fp32)
-//   1 top-k           RMS of x, the pre-norms, softmax, top-8, renormalise, per_expert_scale,
-//                     per-CTA expert counts -> offsets, bases and the token-tile list
-//   2 scatter         stable counting-sort scatter of the 8T slots by expert
-//   3 gate_up GEMM    tcgen05 grouped GEMM, h = gelu_tanh(gate) * up (experts + shared MLP)
-//   4 down GEMM       tcgen05 grouped GEMM, y = w * down(h) (experts), d = down(h) (shared MLP)
-//   5 combine         per token: sum of its 8 y rows, the post-norms, residual, layer_scalar
+// One forward of T tokens queues seven kernels on the caller's stream (programmatic dependent
+// launch, so each one's launch and prologue overlap the previous one's tail), in this order:
+//   0 router prep     W_r * (1 + router_norm_w) split into three bf16 parts
+//   1 router logits   fp32-accurate partial projections on the tensor cores ("The
+//                     architecture": own RMSNorm, a scale, softmax over 128 experts in fp32)
+//   2 top-k           RMS of x, the pre-norms, softmax, top-8, renormalise, per_expert_scale,
+//                     expert counts per 256-token chunk -> offsets, bases and the token-tile list
+//   3 scatter         stable counting-sort scatter of the 8T slots by expert
+//   4 gate_up GEMM    tcgen05 grouped GEMM, h = gelu_tanh(gate) * up (experts + shared MLP)
+//   5 down GEMM       tcgen05 grouped GEMM, y = w * down(h) (experts), d = down(h) (shared MLP)
+//   6 combine         per token: sum of its 8 y rows, the post-norms, residual, layer_scalar
 // Nothing is read back to the host; the GEMMs size their work from device-side counts.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 
-#include "../../include/moe_ffn.h"
+#include "moe_ffn.h"
 #include "internal.h"
 
 using namespace moe;
@@ -56,16 +58,17 @@ bool encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Largest split of the router projection that keeps the router grid near two CTAs per SM of a
-// 152-SM part; a fixed rule so the workspace size does not depend on the device.
+// Split of the router projection over the hidden dimension (a divisor of its 44 chunks of 64):
+// the largest that keeps the router grid within two CTAs per SM of a 152-SM part. A fixed rule, so
+// the workspace size does not depend on the device.
 int choose_ks(int T) {
   static const int opts[] = {44, 22, 11, 4, 2, 1};
-  const int tiles = ((T + kRouterTok - 1) / kRouterTok) * (E / kRouterExp);
+  const int tiles = (T + kRouterN - 1) / kRouterN;
   for (int o : opts)
-    if (tiles * o <= 352) return o;
+    if (tiles * o <= 304) return o;
   return 1;
 }
-constexpr size_t kPartRowsSmall = 5632;  // max ks * T over the T where ks > 1
+constexpr size_t kPartRowsSmall = 304 * kRouterN;  // max ks * T over the T where ks > 1
 
 int choose_tpw(int T) {
   int tpw = 1;
@@ -82,7 +85,7 @@ int choose_bn(int T) {
 
 struct Layout {
   size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, n_exp_tiles, done_ctr, exp_tiles,
-      perm, w_sorted, slot_pos, n1, n2, h, h_dense, y, d, status, total;
+      perm, w_sorted, slot_pos, n1, n2, h, h_dense, y, d, status, wsplit, total;
   int max_tiles;
 };
 
@@ -118,8 +121,9 @@ Layout make_layout(const moe_ffn_config& c) {
   L.n2 = take(Tm * H * 2);
   L.h = take(S * I * 2);
   L.h_dense = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * D * 2 : 0);
-  L.y = take(S * H * 4);
+  L.y = take(S * H * 2);
   L.d = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * H * 4 : 0);
+  L.wsplit = take(static_cast<size_t>(3) * E * H * 2);
   L.total = o;
   return L;
 }
@@ -141,7 +145,9 @@ struct moe_ffn_ctx {
   uint8_t* ws;
   size_t ws_bytes;
   Buffers buf;
-  CUtensorMap map_n1, map_n2, map_h, map_hd;
+  // token-operand maps, one per token-tile width (box rows = BN): n1, h, h_dense
+  CUtensorMap map_n1[4], map_h[4], map_hd[4];
+  CUtensorMap map_wsplit;  // the router's split matrix, boxes of 64 x 128 rows
   // weight maps, re-encoded when the weight pointers change
   const void* cached_gate_up;
   const void* cached_down;
@@ -149,8 +155,8 @@ struct moe_ffn_ctx {
   const void* cached_dense_up;
   const void* cached_dense_down;
   CUtensorMap map_gate_up, map_down, map_dense_gate, map_dense_up, map_dense_down;
-  cudaEvent_t ev_start[6];
-  cudaEvent_t ev_stop[6];
+  cudaEvent_t ev_start[kKernelsPerForward];
+  cudaEvent_t ev_stop[kKernelsPerForward];
   int last_T;
 };
 
@@ -190,7 +196,7 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
     return MOE_FFN_ECUDA;
   if (major != 10 || minor != 3) return MOE_FFN_EARCH;
   if (!get_encode()) return MOE_FFN_ECUDA;
-  if (gemm_set_smem_limits() != cudaSuccess) return MOE_FFN_ECUDA;
+  if (gemm_set_smem_limits() != cudaSuccess || router_set_smem_limit() != cudaSuccess) return MOE_FFN_ECUDA;
 
   moe_ffn_ctx* c = new (std::nothrow) moe_ffn_ctx();
   if (!c) return MOE_FFN_ECUDA;
@@ -221,17 +227,22 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
   b.n2 = reinterpret_cast<uint16_t*>(w + L.n2);
   b.h = reinterpret_cast<uint16_t*>(w + L.h);
   b.h_dense = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<uint16_t*>(w + L.h_dense) : nullptr;
-  b.y = reinterpret_cast<float*>(w + L.y);
+  b.y = reinterpret_cast<uint16_t*>(w + L.y);
   b.d = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<float*>(w + L.d) : nullptr;
+  b.wsplit = reinterpret_cast<uint16_t*>(w + L.wsplit);
   b.max_tiles = L.max_tiles;
 
   const uint64_t Tm = static_cast<uint64_t>(cfg->max_tokens);
-  bool ok = encode_bf16(&c->map_n2, b.n2, Tm, H, 1) && encode_bf16(&c->map_h, b.h, Tm * K, I, 1);
-  if (cfg->mode == MOE_FFN_FULL_LAYER)
-    ok = ok && encode_bf16(&c->map_n1, b.n1, Tm, H, 1) && encode_bf16(&c->map_hd, b.h_dense, Tm, D, 1);
-  else {
-    c->map_n1 = c->map_n2;
-    c->map_hd = c->map_h;
+  bool ok = encode_bf16(&c->map_wsplit, b.wsplit, 3 * E, H, 128);
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t bn = 32u << k;
+    ok = ok && encode_bf16(&c->map_h[k], b.h, Tm * K, I, bn);
+    if (cfg->mode == MOE_FFN_FULL_LAYER)
+      ok = ok && encode_bf16(&c->map_n1[k], b.n1, Tm, H, bn) && encode_bf16(&c->map_hd[k], b.h_dense, Tm, D, bn);
+    else {
+      c->map_n1[k] = c->map_h[k];
+      c->map_hd[k] = c->map_h[k];
+    }
   }
   // The small control words start at zero; the kernels keep them consistent afterwards.
   if (!ok || cudaMemset(w + L.hist, 0, L.exp_tiles - L.hist) != cudaSuccess ||
@@ -264,11 +275,11 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
                     (!full || (c->cached_dense_gate == w->dense_gate && c->cached_dense_up == w->dense_up &&
                                c->cached_dense_down == w->dense_down));
   if (same) return MOE_FFN_OK;
-  bool ok = encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 16) &&
+  bool ok = encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
             encode_bf16(&c->map_down, w->down, static_cast<uint64_t>(E) * H, I, 128);
   if (full)
-    ok = ok && encode_bf16(&c->map_dense_gate, w->dense_gate, D, H, 16) &&
-         encode_bf16(&c->map_dense_up, w->dense_up, D, H, 16) &&
+    ok = ok && encode_bf16(&c->map_dense_gate, w->dense_gate, D, H, 64) &&
+         encode_bf16(&c->map_dense_up, w->dense_up, D, H, 64) &&
          encode_bf16(&c->map_dense_down, w->dense_down, H, D, 128);
   else {
     c->map_dense_gate = c->map_gate_up;
@@ -333,17 +344,18 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   cp.full_layer = rp.full_layer;
   cp.eps = c->cfg.eps;
 
+  const int bk = rp.bn == 32 ? 0 : rp.bn == 64 ? 1 : rp.bn == 128 ? 2 : 3;
   GemmMaps gu, dn;
   gu.a_exp = c->map_gate_up;
   gu.a_dense0 = c->map_dense_gate;
   gu.a_dense1 = c->map_dense_up;
-  gu.b_exp = c->map_n2;
-  gu.b_dense = c->map_n1;
+  gu.b_exp = c->map_n1[bk];  // unused: the experts' gate_up rows are gathered with cp.async
+  gu.b_dense = c->map_n1[bk];
   dn.a_exp = c->map_down;
   dn.a_dense0 = c->map_dense_down;
   dn.a_dense1 = c->map_dense_down;
-  dn.b_exp = c->map_h;
-  dn.b_dense = c->map_hd;
+  dn.b_exp = c->map_h[bk];
+  dn.b_dense = c->map_hd[bk];
 
   // Persistent GEMM grids: at most one CTA per SM, and no more than an upper bound of the items.
   const int S = T * K;
@@ -356,16 +368,17 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   const int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
 
   cudaError_t e = cudaSuccess;
-  for (int k = 0; k < 6 && e == cudaSuccess; ++k) {
+  for (int k = 0; k < kKernelsPerForward && e == cudaSuccess; ++k) {
     if (c->ev_start[k]) e = cudaEventRecord(c->ev_start[k], s);
     if (e != cudaSuccess) break;
     switch (k) {
-      case 0: e = launch_router_logits(rp, c->buf, s); break;
-      case 1: e = launch_route_topk(rp, c->buf, s); break;
-      case 2: e = launch_route_scatter(rp, c->buf, s); break;
-      case 3: e = launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s); break;
-      case 4: e = launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s); break;
-      case 5: e = launch_combine(cp, c->buf, s); break;
+      case 0: e = launch_router_prep(rp, c->buf, s); break;
+      case 1: e = launch_router_logits(c->map_wsplit, rp, c->buf, s); break;
+      case 2: e = launch_route_topk(rp, c->buf, s); break;
+      case 3: e = launch_route_scatter(rp, c->buf, s); break;
+      case 4: e = launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s); break;
+      case 5: e = launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s); break;
+      case 6: e = launch_combine(cp, c->buf, s); break;
     }
     if (e == cudaSuccess && c->ev_stop[k]) e = cudaEventRecord(c->ev_stop[k], s);
   }
@@ -409,7 +422,7 @@ int moe_ffn_device_status(moe_ffn_ctx* c, void* stream, uint32_t* word) {
 }
 
 int moe_ffn_set_kernel_events(moe_ffn_ctx* c, int kernel, void* start, void* stop) {
-  if (!c || kernel < 0 || kernel >= 6) return MOE_FFN_EINVAL;
+  if (!c || kernel < 0 || kernel >= kKernelsPerForward) return MOE_FFN_EINVAL;
   if ((start == nullptr) != (stop == nullptr)) return MOE_FFN_EINVAL;
   c->ev_start[kernel] = static_cast<cudaEvent_t>(start);
   c->ev_stop[kernel] = static_cast<cudaEvent_t>(stop);
@@ -418,7 +431,7 @@ int moe_ffn_set_kernel_events(moe_ffn_ctx* c, int kernel, void* start, void* sto
 
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* c, int T) {
   if (!c || T < 0) return MOE_FFN_EINVAL;
-  return T == 0 ? 0 : 6;
+  return T == 0 ? 0 : kKernelsPerForward;
 }
 
 }  // extern "C"

@@ -1,5 +1,5 @@
-// route.cu — the CUDA-core kernels of the block: router projection, top-k with the pre-norms,
-// the counting-sort scatter of token slots by expert, and the combine with the post-norms.
+// route.cu — the CUDA-core kernels of the block: top-k with the pre-norms, the counting-sort
+// scatter of token slots by expert, and the combine with the post-norms.
 //
 // What they compute follows "Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS Inferentia2 —
 // where every rank weighted the wrong experts", section "The architecture: a dual-path FFN nobody
@@ -33,80 +33,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
-}
-
-// ------------------------------------------------------------------------------------------
-// K1: partial router logits. part[ks][t][e] = sum over the ks-th slice of h of
-// x[t,h] * (1 + router_norm_w[h]) * W_r[e,h]. The RMS factor and the scalar scale are applied
-// after the split sum, in the top-k kernel. fp32 FFMA throughout: the top-8 choice must be taken
-// on fp32 logits.
-__global__ void __launch_bounds__(256) router_logits_kernel(RouteParams p, Buffers b) {
-  __shared__ float xs[kRouterTok][kRouterKc + 1];
-  __shared__ float ws[kRouterExp][kRouterKc + 1];
-  const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * kRouterTok, e0 = blockIdx.y * kRouterExp, ks = blockIdx.z;
-  const int ks_len = H / p.ks;
-  const int kbeg = ks * ks_len;
-  const int ty = tid >> 4, tx = tid & 15;
-  pdl_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) *b.done_ctr = 0;
-
-  float acc[2][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-
-  for (int kc = kbeg; kc < kbeg + ks_len; kc += kRouterKc) {
-    {  // x tile: 32 tokens x 64 columns, 8 bf16 per thread
-      const int r = tid >> 3, c = (tid & 7) * 8;
-      const int t = t0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < p.T) v = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + kc + c);
-      const float4 g0 = *reinterpret_cast<const float4*>(p.router_norm_w + kc + c);
-      const float4 g1 = *reinterpret_cast<const float4*>(p.router_norm_w + kc + c + 4);
-      xs[r][c + 0] = bf16_lo(v.x) * (1.0f + g0.x);
-      xs[r][c + 1] = bf16_hi(v.x) * (1.0f + g0.y);
-      xs[r][c + 2] = bf16_lo(v.y) * (1.0f + g0.z);
-      xs[r][c + 3] = bf16_hi(v.y) * (1.0f + g0.w);
-      xs[r][c + 4] = bf16_lo(v.z) * (1.0f + g1.x);
-      xs[r][c + 5] = bf16_hi(v.z) * (1.0f + g1.y);
-      xs[r][c + 6] = bf16_lo(v.w) * (1.0f + g1.z);
-      xs[r][c + 7] = bf16_hi(v.w) * (1.0f + g1.w);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // W tile: 64 experts x 64 columns, 16 floats per thread
-      const int idx = tid + 256 * i;
-      const int r = idx >> 4, c = (idx & 15) * 4;
-      const float4 v = *reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e0 + r) * H + kc + c);
-      ws[r][c + 0] = v.x;
-      ws[r][c + 1] = v.y;
-      ws[r][c + 2] = v.z;
-      ws[r][c + 3] = v.w;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kRouterKc; ++kk) {
-      const float a0 = xs[2 * ty][kk], a1 = xs[2 * ty + 1][kk];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float w = ws[tx + 16 * j][kk];
-        acc[0][j] = fmaf(a0, w, acc[0][j]);
-        acc[1][j] = fmaf(a1, w, acc[1][j]);
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int t = t0 + 2 * ty + i;
-    if (t < p.T) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        b.logits_part[(static_cast<size_t>(ks) * p.T + t) * E + e0 + tx + 16 * j] = acc[i][j];
-    }
-  }
-  pdl_launch_dependents();
 }
 
 // Warp arg-max over (logit, expert) pairs: larger logit first, lower expert id on equal logits.
@@ -200,14 +126,33 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
     }
 
     // Logits: expert e = lane + 32 j, partial sums added in ascending split order.
+    // Partial sums of the 4 experts of this lane, added in ascending split order, with 32 loads
+    // in flight at a time.
     float lg[4], pr[4];
+    {
+      const float* pp = b.logits_part + static_cast<size_t>(t) * E + lane;
+      const size_t stride = static_cast<size_t>(p.T) * E;
+      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      int s = 0;
+      for (; s + 8 <= p.ks; s += 8) {
+        float a[8][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = lane + 32 * j;
-      float z = 0.0f;
-      for (int s = 0; s < p.ks; ++s) z += b.logits_part[(static_cast<size_t>(s) * p.T + t) * E + e];
-      lg[j] = z * inv * p.router_scale;
-      b.logits[static_cast<size_t>(t) * E + e] = lg[j];
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a[u][j] = pp[(s + u) * stride + 32 * j];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) z[j] += a[u][j];
+      }
+      for (; s < p.ks; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[j] += pp[s * stride + 32 * j];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lg[j] = z[j] * inv * p.router_scale;
+        b.logits[static_cast<size_t>(t) * E + lane + 32 * j] = lg[j];
+      }
     }
     const float m = warp_max(fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3])));
     float zsum = 0.0f;
@@ -279,7 +224,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
 
   // Per-CTA counts, then the last CTA to arrive builds the offsets, bases and tile list.
   __syncthreads();
-  if (tid < E) b.hist[blockIdx.x * E + tid] = hist_s[tid];
+  // Counts per 256-token chunk (the scatter kernel's unit); integer adds, so the totals do not
+  // depend on the order in which CTAs arrive.
+  if (tid < E && hist_s[tid] != 0) atomicAdd(b.hist + ((blockIdx.x * tb) / kScatterTok) * E + tid, hist_s[tid]);
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -290,7 +237,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
   if (!is_last) return;
   __threadfence();
 
-  const int nb = gridDim.x;
+  const int nb = (p.T + kScatterTok - 1) / kScatterTok;  // chunks
   const int e = tid & (E - 1), half = tid >> 7;
   const int bmid = (nb + 1) / 2;
   const int blo = half ? bmid : 0, bhi = half ? nb : bmid;
@@ -399,8 +346,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteParams p, Buffe
   }
   __syncthreads();
   if (!valid) return;
-  const int tb = 8 * p.tpw;
-  const int b0 = (blockIdx.x * kScatterTok) / tb;
+  const int b0 = blockIdx.x;
   const uint32_t lt = (1u << lane) - 1u;
   const int S = p.T * K;
 #pragma unroll
@@ -452,13 +398,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
   float moe[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) moe[j] = 0.0f;
+  uint4 yv[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) yv[k] = *reinterpret_cast<const uint4*>(b.y + static_cast<size_t>(pos_s[k]) * H + f);
 #pragma unroll
   for (int k = 0; k < K; ++k) {
-    const float* yr = b.y + static_cast<size_t>(pos_s[k]) * H + f;
-    const float4 a = *reinterpret_cast<const float4*>(yr);
-    const float4 c = *reinterpret_cast<const float4*>(yr + 4);
-    moe[0] += a.x; moe[1] += a.y; moe[2] += a.z; moe[3] += a.w;
-    moe[4] += c.x; moe[5] += c.y; moe[6] += c.z; moe[7] += c.w;
+    const uint32_t w4[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      moe[2 * j] += bf16_lo(w4[j]);
+      moe[2 * j + 1] += bf16_hi(w4[j]);
+    }
   }
   uint4 o;
   if (!p.full_layer) {
@@ -509,26 +459,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 
 }  // namespace
 
-cudaError_t launch_router_logits(const RouteParams& p, const Buffers& b, cudaStream_t s) {
-  dim3 grid((p.T + kRouterTok - 1) / kRouterTok, E / kRouterExp, p.ks);
-  router_logits_kernel<<<grid, 256, 0, s>>>(p, b);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s) {
   const int tb = 8 * p.tpw;
-  route_topk_kernel<<<(p.T + tb - 1) / tb, 256, 0, s>>>(p, b);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel, dim3((p.T + tb - 1) / tb), dim3(256), 0, s, p, b);
 }
 
 cudaError_t launch_route_scatter(const RouteParams& p, const Buffers& b, cudaStream_t s) {
-  route_scatter_kernel<<<(p.T + kScatterTok - 1) / kScatterTok, 256, 0, s>>>(p, b);
-  return cudaGetLastError();
+  return launch_pdl(route_scatter_kernel, dim3((p.T + kScatterTok - 1) / kScatterTok), dim3(256), 0, s, p, b);
 }
 
 cudaError_t launch_combine(const CombineParams& p, const Buffers& b, cudaStream_t s) {
-  combine_kernel<<<p.T, kCombineThreads, 0, s>>>(p, b);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(p.T), dim3(kCombineThreads), 0, s, p, b);
 }
 
 }  // namespace moe
