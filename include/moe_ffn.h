@@ -160,6 +160,27 @@ int moe_ffn_set_kernel_events(moe_ffn_ctx* ctx, int kernel, void* start, void* s
 /* Number of kernels one forward of T tokens launches on the device (0 for T = 0). */
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
 
+/* The block's fp32 router logits, [T, 128], for callers that cannot allocate device memory (code
+ * running under a memory pool or allocator it does not own, a plugin handed only a stream and its
+ * buffers, a real-time path where an allocation is not allowed). The pages have no counterpart to
+ * this entry point; it exists for such callers only.
+ *   x             device pointer, [T, 2816] bf16, the layer input;
+ *   T             0..1024 tokens (above 1024: MOE_FFN_ETOOBIG, nothing queued; 0: no-op);
+ *   router_w      device pointer, [128, 2816] fp32; router_norm_w: device pointer, [2816] fp32;
+ *   router_scale  the scalar on the normed input (2816^-1/2), eps: the RMSNorm epsilon (1e-6);
+ *   logits        device pointer, [T, 128] fp32, written with the same logits moe_ffn_forward
+ *                 computes for the same x and weights (up to fp32 summation order);
+ *   stream        cudaStream_t as void*; the work is queued there, the host is not synchronised.
+ * It allocates nothing: its scratch is one array of about 2.6 MB in device memory that the library
+ * reserves on each GPU it runs on, held until the process exits. Every call shares that array, so
+ * calls whose GPU work overlaps in time (other streams, other host threads) race and corrupt each
+ * other's results; every byte a call reads there is written earlier in the same call, so nothing
+ * needs clearing. It runs on the calling thread's current CUDA device. The first call on a device
+ * looks up the array's device address and builds a TMA descriptor over it; make that first call
+ * before any stream capture. All pointers must be 16-byte aligned (MOE_FFN_EALIGN). */
+int moe_ffn_router_logits_noalloc(const void* x, int T, const float* router_w, const float* router_norm_w,
+                                  float router_scale, float eps, float* logits, void* stream);
+
 /* A static string naming a status code. */
 const char* moe_ffn_status_string(int status);
 

@@ -74,6 +74,9 @@ def lib():
         L.moe_ffn_set_kernel_events.argtypes = [_vp, ctypes.c_int, _vp, _vp]
         L.moe_ffn_kernels_per_forward.restype = ctypes.c_int
         L.moe_ffn_kernels_per_forward.argtypes = [_vp, ctypes.c_int]
+        L.moe_ffn_router_logits_noalloc.restype = ctypes.c_int
+        L.moe_ffn_router_logits_noalloc.argtypes = [_vp, ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                                     _vp, _vp]
         L.moe_ffn_status_string.restype = ctypes.c_char_p
         L.moe_ffn_status_string.argtypes = [ctypes.c_int]
         L.moe_ffn_destroy.restype = None
@@ -139,6 +142,14 @@ def moe_ffn_set_kernel_events(ctx: int, kernel: int, start: int, stop: int) -> i
 
 def moe_ffn_kernels_per_forward(ctx: int, T: int) -> int:
     return lib().moe_ffn_kernels_per_forward(_vp(ctx), int(T))
+
+
+def moe_ffn_router_logits_noalloc(x: int, T: int, router_w: int, router_norm_w: int, router_scale: float,
+                                  eps: float, logits: int, stream: int) -> int:
+    """Router logits [T, 128] fp32 without any device allocation by the library (for callers that
+    cannot allocate); its scratch is a fixed array shared by all calls, see include/moe_ffn.h."""
+    return lib().moe_ffn_router_logits_noalloc(_vp(x), int(T), _vp(router_w), _vp(router_norm_w),
+                                               float(router_scale), float(eps), _vp(logits), _vp(stream))
 
 
 def moe_ffn_destroy(ctx: int) -> None:

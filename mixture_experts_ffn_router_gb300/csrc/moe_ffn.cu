@@ -138,6 +138,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace moe {
+bool encode_bf16_tensor_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return encode_bf16(map, ptr, rows, cols, box_rows);
+}
+}  // namespace moe
+
 struct moe_ffn_ctx {
   moe_ffn_config cfg;
   int device;
