@@ -20,12 +20,14 @@
 // contiguous in memory (the shared MLP's n1 / h_dense, the experts' h in sorted-slot order) one
 // 2-D TMA box of BN rows; for the experts' gate_up input the rows are gathered by token index from
 // n2 with cp.async by four gather warps, which write the same 128-byte-swizzled layout TMA would.
-// A stage holds KC consecutive K chunks of 64 (KC = 2 for narrow token tiles, so each weight row is
-// fetched 256 bytes at a time).
+// A stage holds KC consecutive K chunks of 64 of both operands (KC = 2 for narrow token tiles, so
+// each weight row is fetched 256 bytes at a time); one ring, so the MMA thread waits and commits
+// once per stage. The MMA of a tile is only as wide as its token rows (rounded up to 16), which the
+// producer passes to the MMA thread with each stage.
 //
-// Warp roles: warp 0 TMA producer; warp 1 MMA issuer (one thread); warps 2..5 epilogue, warp w
-// reading TMEM lanes 32*(w%4).. ; gate_up only: warps 6..9 gather. Two TMEM accumulators let the
-// epilogue of one item overlap the main loop of the next.
+// Warp roles: warp 0 loads A, and B when it is a box; warp 1 issues the MMAs (one thread); warps
+// 2..5 run the epilogue, warp w reading TMEM lanes 32*(w%4).. ; gate_up only: warps 6..9 gather B.
+// Two TMEM accumulators let the epilogue of one item overlap the main loop of the next.
 //
 // gate_up epilogue: TMEM lanes 0..63 hold gate, 64..127 up, of features f0..f0+63. The warps of
 // quarters q and q+2 hold gate and up of the same 32 features; each hands half of its columns to
@@ -43,7 +45,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;                    // bf16 elements per 128-byte swizzled row
 constexpr int kAChunk = kBM * kBK * 2;     // 16 KB of A per K chunk
-constexpr int kStageBudget = 204800;       // shared memory for the stage ring
+constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 
 template <int BN, bool GATE_UP>
 struct Cfg {
@@ -51,7 +53,7 @@ struct Cfg {
   static constexpr int kBChunk = BN * kBK * 2;
   static constexpr int kChunkBytes = kAChunk + kBChunk;
   static constexpr int kStageBytes = KC * kChunkBytes;
-  static constexpr int kStagesRaw = kStageBudget / kStageBytes;
+  static constexpr int kStagesRaw = kRingBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kGatherWarps = GATE_UP ? 4 : 0;
   static constexpr int kThreads = (6 + kGatherWarps) * 32;
@@ -63,12 +65,12 @@ struct Cfg {
   static constexpr int kChunksDense = GATE_UP ? H / kBK : D / kBK; // 44 | 33
   // gate_up: the gate/up hand-over [4 warps][16][32] fp32; down: a 32x32 output chunk per warp.
   static constexpr int kXchgBytes = GATE_UP ? 4 * 16 * 32 * 4 : 4 * 32 * 32 * 4;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kXchgBytes + kBarBytes;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kChunkBytes % 1024 == 0, "operand tiles must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
   static_assert(kStages >= 2, "stages");
+  static_assert(kSmem <= 231424, "shared memory");
 };
 
 struct Item {
@@ -79,28 +81,45 @@ struct Item {
   int m;
 };
 
-// Items: the shared-MLP group first (its items are the longest for the down GEMM), then the
-// experts' token tiles, each followed by its weight tiles in order.
+// Items: the shared-MLP group first (its items are the longest for the down GEMM), then the experts
+// in id order. Within a group the token tiles of one weight tile are consecutive (token tile
+// fastest), so CTAs working at the same time share that weight tile through L2; an expert's items
+// span [11 or 22] x (its token tiles), located with a binary search over tile_off.
 template <int BN, bool GATE_UP>
-__device__ __forceinline__ Item decode_item(int i, int n_dense_items, const int4* tiles, int T) {
+__device__ __forceinline__ Item decode_item(int i, int n_dense_tiles, const int4* tiles, const int* tile_off,
+                                            int T) {
   using C = Cfg<BN, GATE_UP>;
   Item it;
+  const int n_dense_items = n_dense_tiles * C::kMtDense;
   if (i < n_dense_items) {
-    const int j = i / C::kMtDense;
+    const int m = i / n_dense_tiles;
+    const int j = i - m * n_dense_tiles;
     it.dense = 1;
     it.e = E;
-    it.m = i - j * C::kMtDense;
+    it.m = m;
     it.row0 = j * BN;
     it.rows = min(BN, T - j * BN);
   } else {
     const int i2 = i - n_dense_items;
-    const int j = i2 / C::kMtExp;
-    const int4 tt = tiles[j];
+    int lo = 0, hi = E - 1;  // the last expert whose items start at or before i2
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_off[mid] * C::kMtExp <= i2)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int first = tile_off[lo];
+    const int nt = tile_off[lo + 1] - first;
+    const int local = i2 - first * C::kMtExp;
+    const int m = local / nt;
+    const int j = local - m * nt;
+    const int4 tt = tiles[first + j];
     it.dense = 0;
     it.e = tt.x;
     it.row0 = tt.y;
     it.rows = tt.z;
-    it.m = i2 - j * C::kMtExp;
+    it.m = m;
   }
   return it;
 }
@@ -136,7 +155,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);  // [4][16][32]
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kXchgBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
   uint64_t* accf_bar = empty_bar + C::kStages;  // [2] accumulator ready
@@ -144,6 +163,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
   uint64_t* final_bar = acce_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* width_s = reinterpret_cast<int*>(tmem_slot + 2);  // [kStages] MMA width of each stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -180,6 +200,10 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
   pdl_wait();
   const int n_tiles = *reinterpret_cast<volatile int*>(b.n_exp_tiles);
   const int n_dense_tiles = full_layer ? (T + BN - 1) / BN : 0;
+  // Each role decodes items with a binary search over the experts' first tiles; keep them on chip.
+  __shared__ int tile_off_s[E + 1];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) tile_off_s[e] = b.tile_off[e];
+  __syncthreads();
   const int n_dense_items = n_dense_tiles * C::kMtDense;
   const int total = n_dense_items + n_tiles * C::kMtExp;
 
@@ -192,9 +216,10 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
     uint32_t armed = 0, armed_par = 0;  // stages this warp armed, and the parity of the last arm
     bool ok = true;
     for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      const Item it = decode_item<BN, GATE_UP>(i, n_dense_items, b.exp_tiles, T);
+      const Item it = decode_item<BN, GATE_UP>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
       const bool b_tma = !GATE_UP || it.dense;
+      const int width = min(BN, (it.rows + 15) & ~15);
       for (int c0 = 0; c0 < nch; c0 += C::KC) {
         if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
@@ -205,6 +230,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
           uint8_t* st = stages + stage * C::kStageBytes;
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          width_s[stage] = width;
           mbar_arrive_expect_tx(&full_bar[stage], nck * (kAChunk + (b_tma ? C::kBChunk : 0)));
           for (int cc = 0; cc < nck; ++cc) {
             uint8_t* a_dst = st + cc * C::kChunkBytes;
@@ -237,7 +263,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
     // Before the CTA can exit, every TMA load this warp issued must have landed.
     if (lane == 0)
       for (int s2 = 0; s2 < C::kStages; ++s2)
-        if (armed & (1u << s2)) mbar_wait_timeout(&full_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs);
+        if (armed & (1u << s2)) mbar_wait_timeout(&full_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs, b.status);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (one thread)
@@ -252,6 +278,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
         if (!mbar_wait_bounded(&acce_bar[acc], acc_phase ^ 1u, abort_flag, b.status, kStatusWaitAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        uint32_t idesc = 0;
         for (int c0 = 0; c0 < nch; c0 += C::KC) {
           if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, b.status, kStatusWaitFull)) {
             ok = false;
@@ -261,6 +288,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
           // the async proxy.
           if (GATE_UP) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after();
+          // The MMA is only as wide as the tile's token rows (rounded up to the MMA's step of 16).
+          if (c0 == 0) idesc = idesc_bf16_f32(kBM, width_s[stage]);
           const int nck = min(C::KC, nch - c0);
           const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
           for (int cc = 0; cc < nck; ++cc) {
@@ -268,7 +297,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
             const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + kAChunk);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::kIdesc, (c0 | cc | k) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (c0 | cc | k) != 0 ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
@@ -283,7 +312,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
       }
       // All MMAs issued above complete before this barrier's phase does.
       umma_commit(final_bar);
-      mbar_wait_timeout(final_bar, 0, kSpinLimitNs);
+      mbar_wait_timeout(final_bar, 0, kSpinLimitNs, b.status);
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -292,7 +321,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
-      const Item it = decode_item<BN, GATE_UP>(i, n_dense_items, b.exp_tiles, T);
+      const Item it = decode_item<BN, GATE_UP>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       if (!warp_wait(&accf_bar[acc], acc_phase, abort_flag, b.status, kStatusWaitAccFull)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -311,20 +340,35 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = gate_holder ? v[16 + j] : v[j];
           named_bar_sync(pairbar, 64);
-          const int f = it.m * 64 + 32 * (q & 1) + lane;
           uint16_t* dst = it.dense ? b.h_dense : b.h;
           const int ld = it.dense ? D : I;
           const int keep = gate_holder ? 0 : 16;
+          float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float other = theirs[j * 32 + lane];
             const float own = gate_holder ? v[j] : v[16 + j];
             const float g = gate_holder ? own : other;
             const float u = gate_holder ? other : own;
-            const int col = c * 32 + keep + j;
-            if (col < it.rows) dst[static_cast<size_t>(it.row0 + col) * ld + f] = f32_to_bf16_rn(gelu_tanh_approx(g) * u);
+            hv[j] = gelu_tanh_approx(g) * u;
           }
           named_bar_sync(pairbar, 64);
+          // h of 16 token columns x the warp's 32 features goes through shared memory (the warp's
+          // own hand-over slot, free again) so that the global stores are 16-byte vectors.
+          uint16_t* hs = reinterpret_cast<uint16_t*>(mine);  // [16 columns][32 features]
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hs[j * 32 + lane] = f32_to_bf16_rn(hv[j]);
+          __syncwarp();
+          const int f0 = it.m * 64 + 32 * (q & 1);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int idx = lane + 32 * i, r = idx >> 2, c8 = idx & 3;
+            const int col = c * 32 + keep + r;
+            if (col < it.rows)
+              *reinterpret_cast<uint4*>(dst + static_cast<size_t>(it.row0 + col) * ld + f0 + 8 * c8) =
+                  *reinterpret_cast<const uint4*>(hs + r * 32 + 8 * c8);
+          }
+          __syncwarp();
         } else {
           // The warp's 32 features x 32 token columns go through shared memory so that the global
           // stores are 16-byte vectors along the feature dimension.
@@ -379,7 +423,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      const Item it = decode_item<BN, GATE_UP>(i, n_dense_items, b.exp_tiles, T);
+      const Item it = decode_item<BN, GATE_UP>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
       int src[BN / 16];
 #pragma unroll

@@ -33,7 +33,8 @@ struct Buffers {
   int32_t* offsets;     // [129]
   int32_t* n_exp_tiles; // [1]
   int32_t* done_ctr;    // [1]
-  int4* exp_tiles;      // [max_tiles] (expert, first sorted row, rows, 0)
+  int4* exp_tiles;      // [max_tiles] (expert, first sorted row, rows, 0), grouped by expert
+  int32_t* tile_off;    // [129] index of each expert's first token tile in exp_tiles
   int32_t* perm;        // [S]
   float* w_sorted;      // [S]
   int32_t* slot_pos;    // [Tm, 8]

@@ -70,10 +70,11 @@ int choose_ks(int T) {
 }
 constexpr size_t kPartRowsSmall = 304 * kRouterN;  // max ks * T over the T where ks > 1
 
+// Tokens per warp of the top-k kernel: one (its expert counts go to 256-token chunks, so the
+// number of CTAs is not bounded).
 int choose_tpw(int T) {
-  int tpw = 1;
-  while ((T + 8 * tpw - 1) / (8 * tpw) > kMaxRouteBlocks && tpw < 32) tpw *= 2;
-  return tpw;
+  (void)T;
+  return 1;
 }
 
 int choose_bn(int T) {
@@ -84,7 +85,8 @@ int choose_bn(int T) {
 }
 
 struct Layout {
-  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, n_exp_tiles, done_ctr, exp_tiles,
+  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, tile_off, n_exp_tiles, done_ctr,
+      exp_tiles,
       perm, w_sorted, slot_pos, n1, n2, h, h_dense, y, d, status, wsplit, total;
   int max_tiles;
 };
@@ -110,6 +112,7 @@ Layout make_layout(const moe_ffn_config& c) {
   L.base = take(static_cast<size_t>(kMaxRouteBlocks) * E * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
+  L.tile_off = take((E + 1) * 4);
   L.n_exp_tiles = take(4);
   L.done_ctr = take(4);
   L.status = take(4);
@@ -222,6 +225,7 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
   b.base = reinterpret_cast<int32_t*>(w + L.base);
   b.counts = reinterpret_cast<int32_t*>(w + L.counts);
   b.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  b.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
   b.n_exp_tiles = reinterpret_cast<int32_t*>(w + L.n_exp_tiles);
   b.done_ctr = reinterpret_cast<int32_t*>(w + L.done_ctr);
   b.status = reinterpret_cast<unsigned int*>(w + L.status);

@@ -18,6 +18,7 @@ enum : uint32_t {
   kStatusWaitAccEmpty = 1u << 3,   // MMA warp gave up waiting for a drained accumulator
   kStatusBadIndex = 1u << 4,       // an index read from the workspace was out of range
   kStatusBadSchedule = 1u << 5,    // a tile list larger than its buffer
+  kStatusDrain = 1u << 6,          // an exit drain gave up waiting for work already in flight
 };
 
 constexpr unsigned long long kSpinLimitNs = 2000000000ull;  // 2 s
@@ -84,13 +85,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // Waits for the phase with the given parity, giving up after `limit_ns` regardless of any abort
-// flag (used to drain work already in flight before a CTA exits).
-__device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+// flag (used to drain work already in flight before a CTA exits). Giving up sets kStatusDrain.
+__device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity, unsigned long long limit_ns,
+                                                  unsigned int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u && global_ns() - t0 > limit_ns) return false;
+    if ((i & 63u) == 0u && global_ns() - t0 > limit_ns) {
+      atomicOr(status, kStatusDrain);
+      return false;
+    }
   }
 }
 

@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
       tscan_s[ee] = tex;
       b.counts[ee] = cnt[j];
       b.offsets[ee] = cex;
+      b.tile_off[ee] = tex;
       cex += cnt[j];
       tex += nt[j];
     }
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
       scan_s[E] = cex;
       tscan_s[E] = tex;
       b.offsets[E] = cex;
+      b.tile_off[E] = tex;
       if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
       *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
     }

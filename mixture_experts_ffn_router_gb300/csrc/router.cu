@@ -39,24 +39,50 @@ static_assert(kBTile % 1024 == 0, "x tile alignment");
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 // One CTA per expert row: W'[e] = W_r[e] * (1 + router_norm_w), split into bf16 hi, mid, lo.
-__global__ void __launch_bounds__(256) router_prep_kernel(RouteParams p, Buffers b) {
+// 352 threads, 8 consecutive elements each (two 16-byte loads, three 16-byte stores).
+constexpr int kPrepThreads = H / 8;
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+}
+
+__global__ void __launch_bounds__(kPrepThreads) router_prep_kernel(RouteParams p, Buffers b) {
   const int e = blockIdx.x;
+  const int h0 = threadIdx.x * 8;
   pdl_wait();
-  for (int h = threadIdx.x; h < H; h += 256) {
-    const float w = p.router_w[static_cast<size_t>(e) * H + h] * (1.0f + p.router_norm_w[h]);
-    const float hi = bf16_round(w);
-    const float r1 = w - hi;  // exact: hi is w rounded to 8 significant bits
-    const float mid = bf16_round(r1);
-    const float lo = r1 - mid;  // exact, and representable in bf16
-    b.wsplit[(0 * E + e) * static_cast<size_t>(H) + h] = f32_to_bf16_rn(hi);
-    b.wsplit[(1 * E + e) * static_cast<size_t>(H) + h] = f32_to_bf16_rn(mid);
-    b.wsplit[(2 * E + e) * static_cast<size_t>(H) + h] = f32_to_bf16_rn(lo);
+  const float4 w0 = *reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e) * H + h0);
+  const float4 w1 = *reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e) * H + h0 + 4);
+  const float4 g0 = *reinterpret_cast<const float4*>(p.router_norm_w + h0);
+  const float4 g1 = *reinterpret_cast<const float4*>(p.router_norm_w + h0 + 4);
+  const float wv[8] = {w0.x * (1.0f + g0.x), w0.y * (1.0f + g0.y), w0.z * (1.0f + g0.z), w0.w * (1.0f + g0.w),
+                       w1.x * (1.0f + g1.x), w1.y * (1.0f + g1.y), w1.z * (1.0f + g1.z), w1.w * (1.0f + g1.w)};
+  float hi[8], mid[8], lo[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    hi[u] = bf16_round(wv[u]);
+    const float r1 = wv[u] - hi[u];  // exact: hi is w rounded to 8 significant bits
+    mid[u] = bf16_round(r1);
+    lo[u] = r1 - mid[u];             // exact, and representable in bf16
   }
+  uint4* dst = reinterpret_cast<uint4*>(b.wsplit + static_cast<size_t>(e) * H + h0);
+  const size_t part = static_cast<size_t>(E) * H / 8;  // one part, in 16-byte units
+  dst[0] = make_uint4(pack2(hi[0], hi[1]), pack2(hi[2], hi[3]), pack2(hi[4], hi[5]), pack2(hi[6], hi[7]));
+  dst[part] = make_uint4(pack2(mid[0], mid[1]), pack2(mid[2], mid[3]), pack2(mid[4], mid[5]), pack2(mid[6], mid[7]));
+  dst[2 * part] = make_uint4(pack2(lo[0], lo[1]), pack2(lo[2], lo[3]), pack2(lo[4], lo[5]), pack2(lo[6], lo[7]));
   pdl_launch_dependents();
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16-byte cp.async; bytes past src_bytes (0 or 16) are written as zeros.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreadsR, 1)
@@ -78,7 +104,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesR; ++s) {
-      mbar_init(&full_bar[s], 2);  // the TMA byte count + the x stores
+      mbar_init(&full_bar[s], 1 + 32);  // the TMA byte count + the producer lanes' x copies
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < kAccR; ++a) {
@@ -124,26 +150,26 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 #pragma unroll
         for (int part = 0; part < 3; ++part) tma_load_2d(st + part * kTile, &map_w, &full_bar[stage], k0, part * E, pol);
       }
-      // x rows t0..t0+63, 16-byte chunks into the 128-byte-swizzled K-major tile; rows past T are 0.
+      // x rows t0..t0+63, 16-byte chunks copied asynchronously into the 128-byte-swizzled K-major
+      // tile (rows past T are zero-filled); each lane's arrival fires when its copies have landed.
+      const uint32_t xs = smem_u32(st + 3 * kTile);
 #pragma unroll
       for (int i = 0; i < (kRouterN * 8) / 32; ++i) {
         const int idx = lane + 32 * i, r = idx >> 3, cc = idx & 7;
         const int t = t0 + r;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (t < p.T) v = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + k0 + cc * 8));
-        *reinterpret_cast<uint4*>(st + 3 * kTile + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+        const uint16_t* src = p.x + static_cast<size_t>(t < p.T ? t : 0) * H + k0 + cc * 8;
+        cp_async16_zfill(xs + r * 128 + ((cc ^ (r & 7)) << 4), src, t < p.T ? 16u : 0u);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full_bar[stage]);
+      cp_async_arrive_noinc(&full_bar[stage]);
       if (++stage == kStagesR) {
         stage = 0;
         phase ^= 1u;
       }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0)
       for (int s2 = 0; s2 < kStagesR; ++s2)
-        if (armed & (1u << s2)) mbar_wait_timeout(&full_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs);
+        if (armed & (1u << s2)) mbar_wait_timeout(&full_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs, b.status);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer: one accumulator per chunk, rotating through kAccR buffers
@@ -176,7 +202,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         }
       }
       umma_commit(final_bar);
-      mbar_wait_timeout(final_bar, 0, kSpinLimitNs);
+      mbar_wait_timeout(final_bar, 0, kSpinLimitNs, b.status);
     }
     __syncwarp();
   } else {
@@ -237,7 +263,7 @@ cudaError_t router_set_smem_limit() {
 }
 
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s) {
-  return launch_pdl(router_prep_kernel, dim3(E), dim3(256), 0, s, p, b);
+  return launch_pdl(router_prep_kernel, dim3(E), dim3(kPrepThreads), 0, s, p, b);
 }
 
 cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s) {
