@@ -45,6 +45,9 @@ WORKLOADS = {
                         desc="Gemma-4 26B-A4B full dual-path FFN layer, prefill T=4096, Zipf(1.1)-scaled router rows"),
     "moe8": dict(full=False, T=8, skew=False, desc="Gemma-4 26B-A4B MoE block only (router + experts), T=8"),
     "layer": dict(full=True, T=None, skew=False, desc="Gemma-4 26B-A4B full dual-path FFN layer, uniform routing"),
+    "stack30": dict(full=True, T=256, skew=False, layers=30,
+                    desc="Gemma-4 26B-A4B 30-layer stack of full dual-path FFN layers (attention omitted), "
+                         "decode T=256, fresh weights per layer, activations carried layer to layer"),
 }
 
 
@@ -270,18 +273,31 @@ def run_ours(args, wl):
     T = wl["T"]
     mode = B.MOE_FFN_FULL_LAYER if wl["full"] else B.MOE_FFN_MOE_ONLY
 
-    w = synth.make_weights(seed=args.seed, device=dev, full_layer=wl["full"], skew=wl["skew"])
+    L = wl.get("layers", 1)
+    # One context per layer, all sharing the first one's workspace (their forwards never overlap).
+    weights = [synth.make_weights(seed=args.seed, layer=l, device=dev, full_layer=wl["full"], skew=wl["skew"])
+               for l in range(L)]
     x = synth.make_x(T, seed=args.seed, device=dev)
-    out = torch.empty_like(x)
-    m = B.MoeFFN(mode, T, device=local)
-    ws = B.weights_struct(w)
+    bufs = [torch.empty_like(x), torch.empty_like(x)]
+    ctxs = [B.MoeFFN(mode, T, device=local)]
+    for _ in range(1, L):
+        ctxs.append(B.MoeFFN(mode, T, device=local, workspace=ctxs[0].workspace))
+    m = ctxs[0]
+    wss = [B.weights_struct(w) for w in weights]
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
+    out = bufs[(L - 1) % 2]
 
-    def step():
-        rc = B.moe_ffn_forward(m.ctx, x.data_ptr(), T, ws, out.data_ptr(), s)
-        if rc != B.MOE_FFN_OK:
-            raise B.MoeFFNError("moe_ffn_forward", rc)
+    def step(x_in=None, sync_each=None):
+        src = x if x_in is None else x_in
+        for l in range(L):
+            dst = bufs[l % 2]
+            rc = B.moe_ffn_forward(ctxs[l].ctx, src.data_ptr(), T, wss[l], dst.data_ptr(), s)
+            if rc != B.MOE_FFN_OK:
+                raise B.MoeFFNError("moe_ffn_forward", rc)
+            if sync_each is not None:
+                sync_each(l)
+            src = dst
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -289,9 +305,15 @@ def run_ours(args, wl):
     rc, word = m.status()
     if rc != B.MOE_FFN_OK:
         raise RuntimeError("device status 0x%x after warm-up" % word)
-    v = m.views()
-    counts = B.view_tensor(v.counts, (E,), torch.int32).cpu().numpy()
-    experts_hit = int((counts > 0).sum())
+    hits = []
+
+    def count_hits(l):
+        torch.cuda.synchronize()
+        c = B.view_tensor(ctxs[l].views().counts, (E,), torch.int32).cpu().numpy()
+        hits.append(int((c > 0).sum()))
+
+    step(sync_each=count_hits)
+    experts_hit = float(np.mean(hits))
 
     # Breakdown pass (untimed): events around every kernel of each forward, to rank the kernels.
     nk = B.moe_ffn_kernels_per_forward(m.ctx, T)
@@ -304,15 +326,17 @@ def run_ours(args, wl):
             b.record(stream)
         return ev
 
+    # Events go on the last layer's context (every layer runs the same kernels).
+    mk = ctxs[-1]
     bd = [event_pairs(nk) for _ in range(n_b)]
     torch.cuda.synchronize()
     for i in range(n_b):
         for k in range(nk):
-            B.moe_ffn_set_kernel_events(m.ctx, k, bd[i][k][0].cuda_event, bd[i][k][1].cuda_event)
+            B.moe_ffn_set_kernel_events(mk.ctx, k, bd[i][k][0].cuda_event, bd[i][k][1].cuda_event)
         step()
     torch.cuda.synchronize()
     for k in range(nk):
-        B.moe_ffn_set_kernel_events(m.ctx, k, None, None)
+        B.moe_ffn_set_kernel_events(mk.ctx, k, None, None)
     kernel_us = {B.KERNEL_NAMES[k]: float(np.mean([bd[i][k][0].elapsed_time(bd[i][k][1]) for i in range(n_b)]) * 1e3)
                  for k in range(nk)}
     gemms = {"gate_up_gemm": B.KERNEL_NAMES.index("gate_up_gemm"), "down_gemm": B.KERNEL_NAMES.index("down_gemm")}
@@ -335,13 +359,13 @@ def run_ours(args, wl):
     wall0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
-        B.moe_ffn_set_kernel_events(m.ctx, dom_k, ev[i][0].cuda_event, ev[i][1].cuda_event)
+        B.moe_ffn_set_kernel_events(mk.ctx, dom_k, ev[i][0].cuda_event, ev[i][1].cuda_event)
         step()
     t_stop.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     barrier(world, dev)
-    B.moe_ffn_set_kernel_events(m.ctx, dom_k, None, None)
+    B.moe_ffn_set_kernel_events(mk.ctx, dom_k, None, None)
     time.sleep(0.25)
     clocks.stop()
     rc, word = m.status()
@@ -380,10 +404,10 @@ def run_ours(args, wl):
         + ((DENSE_GATE_UP_BYTES + DENSE_DOWN_BYTES) if full else 0)
     layer_flops = T * (FLOPS_PER_TOKEN_EXPERTS + (FLOPS_PER_TOKEN_DENSE if full else 0))
     t_roof = max(layer_bytes / (hbm * 1e9), layer_flops / (tc_burst * 1e12))
-    step_s = ms / args.steps / 1e3
+    step_s = ms / args.steps / 1e3 / L  # per layer
     layer = {"bytes": layer_bytes, "flops": layer_flops, "roofline_us": t_roof * 1e6, "step_us": step_s * 1e6,
              "frac": t_roof / step_s, "bound": "hbm" if layer_bytes / (hbm * 1e9) >= layer_flops / (tc_burst * 1e12) else "tensor",
-             "experts_hit": experts_hit}
+             "experts_hit": experts_hit, "layers_per_step": L}
 
     # ---- end to end through the public API with host buffers
     x_host = x.cpu().pin_memory()
@@ -392,7 +416,7 @@ def run_ours(args, wl):
     x_dev = torch.empty_like(x)
     for _ in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        rc = B.moe_ffn_forward(m.ctx, x_dev.data_ptr(), T, ws, out.data_ptr(), s)
+        step(x_in=x_dev)
         out_host.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -400,9 +424,7 @@ def run_ours(args, wl):
     e0.record(stream)
     for _ in range(e_steps):
         x_dev.copy_(x_host, non_blocking=True)
-        rc = B.moe_ffn_forward(m.ctx, x_dev.data_ptr(), T, ws, out.data_ptr(), s)
-        if rc != B.MOE_FFN_OK:
-            raise B.MoeFFNError("moe_ffn_forward", rc)
+        step(x_in=x_dev)
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -413,9 +435,10 @@ def run_ours(args, wl):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = min(T, 64)
-        tps, cores, secs = oracle_tokens_per_s(wl, synth.host_arrays(w), synth.bf16_bits(x), n)
-        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": "first %d tokens of the step's batch, best of 3 (%.2f s each)" % (n, secs)}
+        tps, cores, secs = oracle_tokens_per_s(wl, synth.host_arrays(weights[0]), synth.bf16_bits(x), n)
+        cpu = {"value": tps / L, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "first %d tokens of the step's batch through layer 0, best of 3 (%.2f s each)%s"
+                         % (n, secs, "; the stack rate is that layer rate / %d" % L if L > 1 else "")}
 
     clk = clocks.summary(wall0, wall1)
     if rank == 0:
@@ -425,14 +448,16 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl["desc"], "T": T, "tokens_per_gpu": T, "hidden": H, "experts": E, "top_k": K,
                        "moe_inter": I, "dense_inter": D if wl["full"] else 0,
-                       "l2": "inputs larger than L2 (%.2f GB of weights read per step)" % (layer_bytes / 1e9),
+                       "layers": L,
+                       "l2": "inputs larger than L2 (%.2f GB of weights read per step)" % (layer_bytes * L / 1e9),
                        "parallelism": "replicas (dp%d, no collective)" % world},
             "roofline": roof, "layer_roofline": layer, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": nk * args.steps, "clocks": clk,
+            "gpu_launches": nk * L * args.steps, "clocks": clk,
             "kernels_us": kernel_us, "kernels_us_note": "untimed breakdown pass, %d steps, events around every kernel" % n_b,
         }
         print(json.dumps(line), flush=True)
-    m.close()
+    for c in ctxs:
+        c.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
