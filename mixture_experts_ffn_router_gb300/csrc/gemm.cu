@@ -10,10 +10,11 @@
 // Layout ("swap AB"): the weight rows are the MMA's M side (128 rows per tile) and the tokens its
 // N side (BN per tile), so a decode step with a handful of tokens per expert still streams every
 // weight tile exactly once at full tile height. Work items are (token tile, 128-row weight tile)
-// pairs; the token tiles of the experts come from a device-side list built by the top-k kernel,
-// the shared MLP is one more group over all T tokens. Each CTA is persistent and takes every
-// gridDim-th item; every output element is written by exactly one CTA with a fixed K order, so
-// results are bitwise reproducible.
+// pairs (or, for the widest token tiles, a token tile and two weight tiles); the token tiles of
+// the experts come from a device-side list built by the top-k kernel, the shared MLP is one more
+// group over all T tokens. CTAs are persistent and claim items one at a time from a global
+// counter, so a CTA that drew short items takes more of them; every output element is written by
+// exactly one CTA with a fixed K order, so results are bitwise reproducible.
 //
 // Operand loading. A (weights): 2-D TMA boxes of 64 K-elements (one 128-byte swizzled row) by 64
 // (gate_up: gate rows, then up rows) or 128 (down) rows. B (tokens): when the token rows are
@@ -47,28 +48,41 @@ constexpr int kBK = 64;                    // bf16 elements per 128-byte swizzle
 constexpr int kAChunk = kBM * kBK * 2;     // 16 KB of A per K chunk
 constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 
-template <int BN, bool GATE_UP>
+// MA = weight tiles per work item: 1, or 2 (an M = 256 item: two 128-row weight tiles share each
+// K chunk of the token tile, which cuts the operand bytes per FLOP from (1/128 + 1/BN) to
+// (1/256 + 1/BN) of the row bytes).
+template <int BN, bool GATE_UP, int MA>
 struct Cfg {
   static constexpr int KC = BN <= 64 ? 2 : 1;
+  static constexpr int kAStage = MA * kAChunk;                     // A bytes of one K chunk
   static constexpr int kBChunk = BN * kBK * 2;
-  static constexpr int kChunkBytes = kAChunk + kBChunk;
+  static constexpr int kChunkBytes = kAStage + kBChunk;
   static constexpr int kStageBytes = KC * kChunkBytes;
   static constexpr int kStagesRaw = kRingBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kEpiWarps = 4 * MA;                         // one per TMEM lane quarter and tile
   static constexpr int kGatherWarps = GATE_UP ? 4 : 0;
-  static constexpr int kThreads = (6 + kGatherWarps) * 32;
+  static constexpr int kGatherWarp0 = 2 + kEpiWarps;
+  static constexpr int kThreads = (2 + kEpiWarps + kGatherWarps) * 32;
   static constexpr int kFullArrivals = 1 + kGatherWarps * 32;
-  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int kMtExp = GATE_UP ? I / 64 : H / kBM;        // 11 | 22 weight tiles per expert
-  static constexpr int kMtDense = GATE_UP ? D / 64 : H / kBM;      // 33 | 22
+  static constexpr int kAccCols = MA * BN;                         // TMEM columns of one accumulator set
+  static constexpr int kNAcc = 2 * kAccCols <= 512 ? 2 : 1;        // double-buffered where it fits
+  static constexpr int kTmemColsRaw = kNAcc * kAccCols;
+  static constexpr int kTmemCols = kTmemColsRaw < 32 ? 32 : kTmemColsRaw;
+  static constexpr int kTilesExp = GATE_UP ? I / 64 : H / kBM;     // 11 | 22 weight tiles per expert
+  static constexpr int kTilesDense = GATE_UP ? D / 64 : H / kBM;   // 33 | 22
+  static constexpr int kMtExp = (kTilesExp + MA - 1) / MA;         // items per token tile
+  static constexpr int kMtDense = (kTilesDense + MA - 1) / MA;
   static constexpr int kChunksExp = GATE_UP ? H / kBK : I / kBK;   // 44 | 11 K chunks
   static constexpr int kChunksDense = GATE_UP ? H / kBK : D / kBK; // 44 | 33
-  // gate_up: the gate/up hand-over [4 warps][16][32] fp32; down: a 32x32 output chunk per warp.
-  static constexpr int kXchgBytes = GATE_UP ? 4 * 16 * 32 * 4 : 4 * 32 * 32 * 4;
+  // gate_up: the gate/up hand-over [warps][16][32] fp32; down: a 32x32 output chunk per warp.
+  static constexpr int kXchgBytes = kEpiWarps * (GATE_UP ? 16 * 32 * 4 : 32 * 32 * 4);
   static constexpr int kBarBytes = 512;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kXchgBytes + kBarBytes;
   static_assert(kChunkBytes % 1024 == 0, "operand tiles must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(MA == 1 || MA == 2, "MA");
+  static_assert(kTmemColsRaw <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(kStages >= 2, "stages");
   static_assert(kSmem <= 231424, "shared memory");
 };
@@ -79,16 +93,17 @@ struct Item {
   int row0;
   int rows;
   int m;
+  int nt;  // token tiles of the item's group (expert or shared MLP)
 };
 
 // Items: the shared-MLP group first (its items are the longest for the down GEMM), then the experts
 // in id order. Within a group the token tiles of one weight tile are consecutive (token tile
 // fastest), so CTAs working at the same time share that weight tile through L2; an expert's items
 // span [11 or 22] x (its token tiles), located with a binary search over tile_off.
-template <int BN, bool GATE_UP>
+template <int BN, bool GATE_UP, int MA>
 __device__ __forceinline__ Item decode_item(int i, int n_dense_tiles, const int4* tiles, const int* tile_off,
                                             int T) {
-  using C = Cfg<BN, GATE_UP>;
+  using C = Cfg<BN, GATE_UP, MA>;
   Item it;
   const int n_dense_items = n_dense_tiles * C::kMtDense;
   if (i < n_dense_items) {
@@ -99,6 +114,7 @@ __device__ __forceinline__ Item decode_item(int i, int n_dense_tiles, const int4
     it.m = m;
     it.row0 = j * BN;
     it.rows = min(BN, T - j * BN);
+    it.nt = n_dense_tiles;
   } else {
     const int i2 = i - n_dense_items;
     int lo = 0, hi = E - 1;  // the last expert whose items start at or before i2
@@ -120,6 +136,7 @@ __device__ __forceinline__ Item decode_item(int i, int n_dense_tiles, const int4
     it.row0 = tt.y;
     it.rows = tt.z;
     it.m = m;
+    it.nt = nt;
   }
   return it;
 }
@@ -138,6 +155,42 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Work items are handed out dynamically: the producer warp claims the next item index from a
+// global counter and publishes it in a ring of kItemSlots slots in shared memory; the MMA thread,
+// the epilogue warps and the gather warps read the same sequence from the ring. -1 ends the
+// sequence. Which CTA computes an item varies from run to run, but each item is still computed
+// whole by one CTA in a fixed order, so the results do not.
+constexpr int kItemSlots = 8;
+
+// One consumer (a single thread) takes the next item: its index, -1 at the end, -2 if it gave up.
+__device__ __forceinline__ int next_item(uint64_t* itemf, uint64_t* iteme, const volatile int* item_s, int& slot,
+                                         uint32_t& par, volatile int* abort_flag, unsigned int* status) {
+  int i = -2;
+  if (mbar_wait_bounded(&itemf[slot], par, abort_flag, status, kStatusWaitItem)) {
+    i = item_s[slot];
+    mbar_arrive(&iteme[slot]);
+  }
+  if (++slot == kItemSlots) {
+    slot = 0;
+    par ^= 1u;
+  }
+  return i;
+}
+
+// The same for a whole warp: lane 0 takes the item, the index is broadcast.
+__device__ __forceinline__ int warp_next_item(uint64_t* itemf, uint64_t* iteme, const volatile int* item_s,
+                                              int& slot, uint32_t& par, volatile int* abort_flag,
+                                              unsigned int* status) {
+  int i = -2;
+  if ((threadIdx.x & 31) == 0) {
+    i = next_item(itemf, iteme, item_s, slot, par, abort_flag, status);
+  } else if (++slot == kItemSlots) {
+    slot = 0;
+    par ^= 1u;
+  }
+  return __shfl_sync(0xffffffffu, i, 0);
+}
+
 // Lane 0 waits, the result is broadcast, so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status, uint32_t why) {
@@ -146,24 +199,27 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
-template <int BN, bool GATE_UP>
-__global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
+template <int BN, bool GATE_UP, int MA>
+__global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a_exp, const __grid_constant__ CUtensorMap map_a_d0,
                         const __grid_constant__ CUtensorMap map_a_d1, const __grid_constant__ CUtensorMap map_b_exp,
                         const __grid_constant__ CUtensorMap map_b_dense, Buffers b, int T, int full_layer) {
-  using C = Cfg<BN, GATE_UP>;
+  using C = Cfg<BN, GATE_UP, MA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kXchgBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
-  uint64_t* accf_bar = empty_bar + C::kStages;  // [2] accumulator ready
-  uint64_t* acce_bar = accf_bar + 2;            // [2] accumulator drained
+  uint64_t* accf_bar = empty_bar + C::kStages;  // [kNAcc] accumulator ready
+  uint64_t* acce_bar = accf_bar + 2;            // [kNAcc] accumulator drained
   uint64_t* final_bar = acce_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  uint64_t* itemf_bar = final_bar + 1;          // [kItemSlots] item published
+  uint64_t* iteme_bar = itemf_bar + kItemSlots; // [kItemSlots] item read by every consumer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(iteme_bar + kItemSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* width_s = reinterpret_cast<int*>(tmem_slot + 2);  // [kStages] MMA width of each stage
+  volatile int* item_s = reinterpret_cast<volatile int*>(width_s + 8);  // [kItemSlots] item ring
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -172,11 +228,15 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
       mbar_init(&full_bar[s], C::kFullArrivals);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::kNAcc; ++a) {
       mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], 4);
+      mbar_init(&acce_bar[a], C::kEpiWarps);
     }
     mbar_init(final_bar, 1);
+    for (int k = 0; k < kItemSlots; ++k) {
+      mbar_init(&itemf_bar[k], 1);
+      mbar_init(&iteme_bar[k], 1 + C::kEpiWarps + C::kGatherWarps);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&map_a_exp);
@@ -209,47 +269,99 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
 
   if (warp == 0) {
     // ---------------- producer: TMA loads of A, and of B when its rows are contiguous
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_x = policy_evict_last();
+    // Weight tiles that at least two more token tiles of the same group read again are kept in L2
+    // (evict_last); the rest stream through (evict_first). Keeping tiles with one re-read was
+    // measured slower: the lines stay protected in L2 long after their last use.
+    const uint64_t pol_once = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const uint64_t pol_x = pol_keep;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_par = 0;  // stages this warp armed, and the parity of the last arm
     bool ok = true;
-    for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      const Item it = decode_item<BN, GATE_UP>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+    int* sched = b.sched + (GATE_UP ? 0 : 1);
+    int slot = 0;
+    uint32_t slot_par = 0;
+    // The next item is claimed one ring's depth of stages before the current one is fully issued:
+    // late enough that a CTA busy with a long item does not hold on to work an idle CTA could
+    // take, early enough that the atomic's round trip overlaps the loads still to come.
+    int next = 0;
+    bool have_next = false;
+    while (ok) {
+      int i = -2;
+      if (lane == 0) {
+        if (!have_next) next = atomicAdd(sched, 1);
+        have_next = false;
+        if (mbar_wait_bounded(&iteme_bar[slot], slot_par ^ 1u, abort_flag, b.status, kStatusWaitItem)) {
+          i = next < total ? next : -1;
+          item_s[slot] = i;
+          mbar_arrive(&itemf_bar[slot]);
+        }
+      }
+      i = __shfl_sync(0xffffffffu, i, 0);
+      if (++slot == kItemSlots) {
+        slot = 0;
+        slot_par ^= 1u;
+      }
+      if (i < 0) break;
+      const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
       const bool b_tma = !GATE_UP || it.dense;
       const int width = min(BN, (it.rows + 15) & ~15);
+      const int n_tiles_raw = it.dense ? C::kTilesDense : C::kTilesExp;
+      const int na = min(MA, n_tiles_raw - it.m * MA);  // weight tiles of this item
+      const uint64_t pol_w = it.nt > 2 ? pol_keep : pol_once;
+      // gate_up with two tiles: tile 0 holds the gate rows and tile 1 the up rows of 128 features
+      // ("paired"); otherwise each tile holds the gate and up rows of 64 features ("stacked").
+      const bool paired = GATE_UP && MA == 2 && na == 2;
       for (int c0 = 0; c0 < nch; c0 += C::KC) {
         if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
           break;
         }
         if (lane == 0) {
+          if (!have_next && c0 + C::kStages * C::KC >= nch) {
+            next = atomicAdd(sched, 1);
+            have_next = true;
+          }
           const int nck = min(C::KC, nch - c0);
           uint8_t* st = stages + stage * C::kStageBytes;
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          width_s[stage] = width;
-          mbar_arrive_expect_tx(&full_bar[stage], nck * (kAChunk + (b_tma ? C::kBChunk : 0)));
+          width_s[stage] = width | (na << 16);
+          mbar_arrive_expect_tx(&full_bar[stage], nck * (na * kAChunk + (b_tma ? C::kBChunk : 0)));
           for (int cc = 0; cc < nck; ++cc) {
             uint8_t* a_dst = st + cc * C::kChunkBytes;
             const int k0 = (c0 + cc) * kBK;
-            if (GATE_UP) {
+            if (paired) {
               const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
               const CUtensorMap* mu = it.dense ? &map_a_d1 : &map_a_exp;
-              const int grow = it.dense ? it.m * 64 : it.e * (2 * I) + it.m * 64;
-              const int urow = it.dense ? it.m * 64 : it.e * (2 * I) + I + it.m * 64;
+              const int f0 = it.m * 128;
+              const int grow = it.dense ? f0 : it.e * (2 * I) + f0;
+              const int urow = it.dense ? f0 : it.e * (2 * I) + I + f0;
               tma_load_2d(a_dst, mg, &full_bar[stage], k0, grow, pol_w);
-              tma_load_2d(a_dst + kAChunk / 2, mu, &full_bar[stage], k0, urow, pol_w);
-            } else {
-              const CUtensorMap* ma = it.dense ? &map_a_d0 : &map_a_exp;
-              const int arow = it.dense ? it.m * kBM : it.e * H + it.m * kBM;
-              tma_load_2d(a_dst, ma, &full_bar[stage], k0, arow, pol_w);
+              tma_load_2d(a_dst + kAChunk / 2, mg, &full_bar[stage], k0, grow + 64, pol_w);
+              tma_load_2d(a_dst + kAChunk, mu, &full_bar[stage], k0, urow, pol_w);
+              tma_load_2d(a_dst + kAChunk + kAChunk / 2, mu, &full_bar[stage], k0, urow + 64, pol_w);
+            }
+            for (int a = 0; a < (paired ? 0 : na); ++a) {
+              const int tile = it.m * MA + a;
+              if (GATE_UP) {
+                const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
+                const CUtensorMap* mu = it.dense ? &map_a_d1 : &map_a_exp;
+                const int grow = it.dense ? tile * 64 : it.e * (2 * I) + tile * 64;
+                const int urow = it.dense ? tile * 64 : it.e * (2 * I) + I + tile * 64;
+                tma_load_2d(a_dst + a * kAChunk, mg, &full_bar[stage], k0, grow, pol_w);
+                tma_load_2d(a_dst + a * kAChunk + kAChunk / 2, mu, &full_bar[stage], k0, urow, pol_w);
+              } else {
+                const CUtensorMap* mp = it.dense ? &map_a_d0 : &map_a_exp;
+                const int arow = it.dense ? tile * kBM : it.e * H + tile * kBM;
+                tma_load_2d(a_dst + a * kAChunk, mp, &full_bar[stage], k0, arow, pol_w);
+              }
             }
             if (b_tma) {
               const CUtensorMap* mb = it.dense ? &map_b_dense : &map_b_exp;
-              tma_load_2d(a_dst + kAChunk, mb, &full_bar[stage], k0, it.row0, pol_x);
+              tma_load_2d(a_dst + C::kAStage, mb, &full_bar[stage], k0, it.row0, pol_x);
             }
           }
         }
@@ -273,12 +385,17 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+      int slot = 0;
+      uint32_t slot_par = 0;
+      while (ok) {
+        const int i = next_item(itemf_bar, iteme_bar, item_s, slot, slot_par, abort_flag, b.status);
+        if (i < 0) break;
         const int nch = (i < n_dense_items) ? C::kChunksDense : C::kChunksExp;
         if (!mbar_wait_bounded(&acce_bar[acc], acc_phase ^ 1u, abort_flag, b.status, kStatusWaitAccEmpty)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
         uint32_t idesc = 0;
+        int na = 1;
         for (int c0 = 0; c0 < nch; c0 += C::KC) {
           if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, b.status, kStatusWaitFull)) {
             ok = false;
@@ -289,15 +406,24 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
           if (GATE_UP) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after();
           // The MMA is only as wide as the tile's token rows (rounded up to the MMA's step of 16).
-          if (c0 == 0) idesc = idesc_bf16_f32(kBM, width_s[stage]);
+          if (c0 == 0) {
+            const int ws = width_s[stage];
+            idesc = idesc_bf16_f32(kBM, ws & 0xFFFF);
+            na = ws >> 16;
+          }
           const int nck = min(C::KC, nch - c0);
           const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
           for (int cc = 0; cc < nck; ++cc) {
-            const uint64_t a_desc = smem_desc_sw128(st + cc * C::kChunkBytes);
-            const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + kAChunk);
+            const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + C::kAStage);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (c0 | cc | k) != 0 ? 1u : 0u);
+            for (int a = 0; a < MA; ++a) {
+              if (a >= na) break;
+              const uint64_t a_desc = smem_desc_sw128(st + cc * C::kChunkBytes + a * kAChunk);
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_bf16(d_tmem + static_cast<uint32_t>(a * BN), a_desc + 2u * k, b_desc + 2u * k, idesc,
+                          (c0 | cc | k) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
@@ -307,35 +433,79 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
         }
         if (!ok) break;
         umma_commit(&accf_bar[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == C::kNAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // All MMAs issued above complete before this barrier's phase does.
       umma_commit(final_bar);
       mbar_wait_timeout(final_bar, 0, kSpinLimitNs, b.status);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ---------------- epilogue warps 2..5; TMEM lane quarter = warp % 4
+  } else if (warp < C::kGatherWarp0) {
+    // ---------------- epilogue warps 2..; TMEM lane quarter = warp % 4, weight tile (warp - 2) / 4
     const int q = warp & 3;
+    const int ta = (warp - 2) >> 2;
+    float* xw = xchg + (ta * 4) * (GATE_UP ? 512 : 1024);  // this tile's four hand-over slots
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int i = blockIdx.x; i < total; i += gridDim.x) {
-      const Item it = decode_item<BN, GATE_UP>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+    int slot = 0;
+    uint32_t slot_par = 0;
+    for (;;) {
+      const int i = warp_next_item(itemf_bar, iteme_bar, item_s, slot, slot_par, abort_flag, b.status);
+      if (i < 0) break;
+      const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+      const int tile = it.m * MA + ta;
+      const int n_tiles_raw = it.dense ? C::kTilesDense : C::kTilesExp;
+      const bool has_tile = tile < n_tiles_raw;
+      const bool paired = GATE_UP && MA == 2 && it.m * MA + 1 < n_tiles_raw;
       if (!warp_wait(&accf_bar[acc], acc_phase, abort_flag, b.status, kStatusWaitAccFull)) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (paired) {
+        // Gate (tile 0) and up (tile 1) of features f + lane sit in this warp's own TMEM lanes;
+        // the two warps of a lane quarter split the token columns.
+        const int f = it.m * 128 + 32 * q;
+        const uint32_t t_g = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * C::kAccCols);
+        uint16_t* hs = reinterpret_cast<uint16_t*>(xw + q * 512);  // [32 columns][32 features] bf16
+        uint16_t* dst = it.dense ? b.h_dense : b.h;
+        const int ld = it.dense ? D : I;
+#pragma unroll 1
+        for (int c = ta * (BN / 64); c < (ta + 1) * (BN / 64); ++c) {
+          if (c * 32 >= it.rows) break;
+          uint32_t g[32], u[32];
+          tmem_ld32_nowait(t_g + c * 32, g);
+          tmem_ld32_nowait(t_g + BN + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            hs[j * 32 + lane] = f32_to_bf16_rn(gelu_tanh_approx(__uint_as_float(g[j])) * __uint_as_float(u[j]));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = lane + 32 * i, r = idx >> 2, c8 = idx & 3;
+            const int col = c * 32 + r;
+            if (col < it.rows)
+              *reinterpret_cast<uint4*>(dst + static_cast<size_t>(it.row0 + col) * ld + f + 8 * c8) =
+                  *reinterpret_cast<const uint4*>(hs + r * 32 + 8 * c8);
+          }
+          __syncwarp();
+        }
+      }
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * C::kAccCols + ta * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
-        if (c * 32 >= it.rows) break;
+        if (paired || !has_tile || c * 32 >= it.rows) break;
         float v[32];
         tmem_ld32(t_row + c * 32, v);
         if (GATE_UP) {
           // q 0/1: gate of features f0+32(q&1)+lane; q 2/3: up of the same features.
           const bool gate_holder = q < 2;
-          const int pairbar = 1 + (q & 1);
-          float* mine = xchg + q * 512;
-          const float* theirs = xchg + (q ^ 2) * 512;
+          const int pairbar = 1 + (q & 1) + 2 * ta;
+          float* mine = xw + q * 512;
+          const float* theirs = xw + (q ^ 2) * 512;
           // The gate holder hands over columns 16..31 and finishes 0..15; the up holder the reverse.
 #pragma unroll
           for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = gate_holder ? v[16 + j] : v[j];
@@ -359,7 +529,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) hs[j * 32 + lane] = f32_to_bf16_rn(hv[j]);
           __syncwarp();
-          const int f0 = it.m * 64 + 32 * (q & 1);
+          const int f0 = tile * 64 + 32 * (q & 1);
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const int idx = lane + 32 * i, r = idx >> 2, c8 = idx & 3;
@@ -372,8 +542,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
         } else {
           // The warp's 32 features x 32 token columns go through shared memory so that the global
           // stores are 16-byte vectors along the feature dimension.
-          const int f0 = it.m * kBM + 32 * q;
-          uint8_t* stg = reinterpret_cast<uint8_t*>(xchg) + q * 4096;
+          const int f0 = tile * kBM + 32 * q;
+          uint8_t* stg = reinterpret_cast<uint8_t*>(xw) + q * 4096;
           if (it.dense) {
             float* sd = reinterpret_cast<float*>(stg);  // [32 tokens][32 features]
 #pragma unroll
@@ -411,19 +581,25 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == C::kNAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   } else {
-    // ---------------- gather warps 6..9 (gate_up only): expert token rows of n2 by cp.async
-    const int g = threadIdx.x - 192;         // 0..127
+    // ---------------- gather warps (gate_up only): expert token rows of n2 by cp.async
+    const int g = threadIdx.x - C::kGatherWarp0 * 32;  // 0..127
     const int chunk16 = g & 7;               // which 16 bytes of the 128-byte row
     const int rbase = g >> 3;                // rows rbase, rbase+16, ...
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      const Item it = decode_item<BN, GATE_UP>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+    int slot = 0;
+    uint32_t slot_par = 0;
+    while (ok) {
+      const int i = warp_next_item(itemf_bar, iteme_bar, item_s, slot, slot_par, abort_flag, b.status);
+      if (i < 0) break;
+      const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
       int src[BN / 16];
 #pragma unroll
@@ -448,7 +624,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
           const int nck = min(C::KC, nch - c0);
           const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
           for (int cc = 0; cc < nck; ++cc) {
-            const uint32_t b_dst = st + cc * C::kChunkBytes + kAChunk;
+            const uint32_t b_dst = st + cc * C::kChunkBytes + C::kAStage;
             const int k0 = (c0 + cc) * kBK;
 #pragma unroll
             for (int r = 0; r < BN / 16; ++r) {
@@ -479,41 +655,50 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP>::kThreads, 1)
   }
 }
 
-template <int BN, bool GATE_UP>
+template <int BN, bool GATE_UP, int MA>
 cudaError_t launch_t(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s) {
-  using C = Cfg<BN, GATE_UP>;
-  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
+  using C = Cfg<BN, GATE_UP, MA>;
+  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP, MA>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
                     m.a_dense0, m.a_dense1, m.b_exp, m.b_dense, b, T, full_layer);
 }
 
-template <int BN, bool GATE_UP>
+template <int BN, bool GATE_UP, int MA>
 cudaError_t set_limit() {
-  using C = Cfg<BN, GATE_UP>;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using C = Cfg<BN, GATE_UP, MA>;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GATE_UP, MA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               C::kSmem);
 }
 
 }  // namespace
 
+// Weight tiles per work item of the gate_up GEMM: two for wide token tiles (T above 512), where
+// the operand traffic per FLOP and the epilogue's gate/up hand-over cost more than the longer
+// items do; one for decode-sized T, where the weight stream is the bound and more, shorter items
+// balance better over the SMs. (Two tiles per item were measured slower for the down GEMM, whose
+// short K leaves a single-buffered accumulator's epilogue exposed.)
+int gate_up_tiles_per_item(int bn, int T) { return bn == 256 || (bn == 128 && T > 512) ? 2 : 1; }
+
 cudaError_t gemm_set_smem_limits() {
   cudaError_t e;
-  if ((e = set_limit<32, true>()) != cudaSuccess) return e;
-  if ((e = set_limit<64, true>()) != cudaSuccess) return e;
-  if ((e = set_limit<128, true>()) != cudaSuccess) return e;
-  if ((e = set_limit<256, true>()) != cudaSuccess) return e;
-  if ((e = set_limit<32, false>()) != cudaSuccess) return e;
-  if ((e = set_limit<64, false>()) != cudaSuccess) return e;
-  if ((e = set_limit<128, false>()) != cudaSuccess) return e;
-  return set_limit<256, false>();
+  if ((e = set_limit<32, true, 1>()) != cudaSuccess) return e;
+  if ((e = set_limit<64, true, 1>()) != cudaSuccess) return e;
+  if ((e = set_limit<128, true, 1>()) != cudaSuccess) return e;
+  if ((e = set_limit<128, true, 2>()) != cudaSuccess) return e;
+  if ((e = set_limit<256, true, 2>()) != cudaSuccess) return e;
+  if ((e = set_limit<32, false, 1>()) != cudaSuccess) return e;
+  if ((e = set_limit<64, false, 1>()) != cudaSuccess) return e;
+  if ((e = set_limit<128, false, 1>()) != cudaSuccess) return e;
+  return set_limit<256, false, 1>();
 }
 
 cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                            cudaStream_t s) {
   switch (bn) {
-    case 32: return launch_t<32, true>(m, b, T, full_layer, grid, s);
-    case 64: return launch_t<64, true>(m, b, T, full_layer, grid, s);
-    case 128: return launch_t<128, true>(m, b, T, full_layer, grid, s);
-    case 256: return launch_t<256, true>(m, b, T, full_layer, grid, s);
+    case 32: return launch_t<32, true, 1>(m, b, T, full_layer, grid, s);
+    case 64: return launch_t<64, true, 1>(m, b, T, full_layer, grid, s);
+    case 128: return gate_up_tiles_per_item(bn, T) == 2 ? launch_t<128, true, 2>(m, b, T, full_layer, grid, s)
+                                                        : launch_t<128, true, 1>(m, b, T, full_layer, grid, s);
+    case 256: return launch_t<256, true, 2>(m, b, T, full_layer, grid, s);  // two tiles per item
     default: return cudaErrorInvalidValue;
   }
 }
@@ -521,10 +706,10 @@ cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, i
 cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                         cudaStream_t s) {
   switch (bn) {
-    case 32: return launch_t<32, false>(m, b, T, full_layer, grid, s);
-    case 64: return launch_t<64, false>(m, b, T, full_layer, grid, s);
-    case 128: return launch_t<128, false>(m, b, T, full_layer, grid, s);
-    case 256: return launch_t<256, false>(m, b, T, full_layer, grid, s);
+    case 32: return launch_t<32, false, 1>(m, b, T, full_layer, grid, s);
+    case 64: return launch_t<64, false, 1>(m, b, T, full_layer, grid, s);
+    case 128: return launch_t<128, false, 1>(m, b, T, full_layer, grid, s);
+    case 256: return launch_t<256, false, 1>(m, b, T, full_layer, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

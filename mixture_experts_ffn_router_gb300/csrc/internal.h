@@ -33,6 +33,7 @@ struct Buffers {
   int32_t* offsets;     // [129]
   int32_t* n_exp_tiles; // [1]
   int32_t* done_ctr;    // [1]
+  int32_t* sched;       // [2] work-item counters of the gate_up and down GEMMs (zeroed by top-k)
   int4* exp_tiles;      // [max_tiles] (expert, first sorted row, rows, 0), grouped by expert
   int32_t* tile_off;    // [129] index of each expert's first token tile in exp_tiles
   int32_t* perm;        // [S]
@@ -118,6 +119,7 @@ cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, i
 cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                         cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
+int gate_up_tiles_per_item(int bn, int T);
 cudaError_t router_set_smem_limit();
 
 }  // namespace moe

@@ -85,7 +85,7 @@ int choose_bn(int T) {
 }
 
 struct Layout {
-  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, tile_off, n_exp_tiles, done_ctr,
+  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, tile_off, n_exp_tiles, done_ctr, sched,
       exp_tiles,
       perm, w_sorted, slot_pos, n1, n2, h, h_dense, y, d, status, wsplit, total;
   int max_tiles;
@@ -115,6 +115,7 @@ Layout make_layout(const moe_ffn_config& c) {
   L.tile_off = take((E + 1) * 4);
   L.n_exp_tiles = take(4);
   L.done_ctr = take(4);
+  L.sched = take(8);
   L.status = take(4);
   L.exp_tiles = take(static_cast<size_t>(L.max_tiles) * 16);
   L.perm = take(S * 4);
@@ -228,6 +229,7 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
   b.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
   b.n_exp_tiles = reinterpret_cast<int32_t*>(w + L.n_exp_tiles);
   b.done_ctr = reinterpret_cast<int32_t*>(w + L.done_ctr);
+  b.sched = reinterpret_cast<int32_t*>(w + L.sched);
   b.status = reinterpret_cast<unsigned int*>(w + L.status);
   b.exp_tiles = reinterpret_cast<int4*>(w + L.exp_tiles);
   b.perm = reinterpret_cast<int32_t*>(w + L.perm);
@@ -372,7 +374,9 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   const int bn = rp.bn;
   const int ub_tiles = (S < E ? S : E) + S / bn;
   const int nd = full ? (T + bn - 1) / bn : 0;
-  const long items_gu = static_cast<long>(ub_tiles) * (I / 64) + static_cast<long>(nd) * (D / 64);
+  const int ma = gate_up_tiles_per_item(bn, T);
+  const long items_gu = static_cast<long>(ub_tiles) * ((I / 64 + ma - 1) / ma) +
+                        static_cast<long>(nd) * ((D / 64 + ma - 1) / ma);
   const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
   const int grid_gu = static_cast<int>(items_gu < c->num_sms ? items_gu : c->num_sms);
   const int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);

@@ -288,6 +288,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
       b.tile_off[E] = tex;
       if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
       *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
+      b.sched[0] = 0;  // the GEMMs of this forward claim their work items from these counters
+      b.sched[1] = 0;
     }
   }
   __syncthreads();

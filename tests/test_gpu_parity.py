@@ -71,7 +71,7 @@ def test_full_layer_prefill_skewed_4096():
     assert (load == 0).sum() >= 8             # ... and experts with no tokens
 
 
-@pytest.mark.parametrize("T", [256, 1024, 1500])
+@pytest.mark.parametrize("T", [256, 777, 1024, 1500])
 def test_full_layer_sweep_sizes(T):
     _sampled_check(FULL, T, 400 + T, False, 32, "full T=%d" % T)
 
@@ -97,9 +97,12 @@ def test_all_tokens_identical_pick_the_same_experts():
     G.check_values(run.out_f64[:1], ref["out"], "identical tokens")
 
 
-def test_deterministic_bitwise():
-    x, w = G.make_case(FULL, 500, 700)
-    m = B.MoeFFN(FULL, 500)
+@pytest.mark.parametrize("T", [500, 2048])
+def test_deterministic_bitwise(T):
+    # The GEMMs hand out work items dynamically, so which CTA computes an item differs between
+    # runs; each item is computed whole in a fixed order, so the output may not.
+    x, w = G.make_case(FULL, T, 700)
+    m = B.MoeFFN(FULL, T)
     a = m.forward(x, w).clone()
     b = m.forward(x, w).clone()
     torch.cuda.synchronize()
