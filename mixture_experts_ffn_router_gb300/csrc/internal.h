@@ -13,8 +13,8 @@ constexpr int K = 8;      // experts per token
 constexpr int I = 704;    // expert intermediate width
 constexpr int D = 2112;   // shared-MLP intermediate width
 
-// Router kernel: 64 tokens per CTA (the MMA's N), the hidden dimension split into `ks` parts.
-constexpr int kRouterN = 64;
+// Router kernel: 128 tokens per CTA (the MMA's N), the hidden dimension split into `ks` parts.
+constexpr int kRouterN = 128;
 // Token-scatter kernel: 256 tokens per CTA (8 warps of 32).
 constexpr int kScatterTok = 256;
 // Combine kernel: one CTA per token, 352 threads x 8 features.

@@ -59,16 +59,18 @@ bool encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Split of the router projection over the hidden dimension (a divisor of its 44 chunks of 64):
-// the largest that keeps the router grid within two CTAs per SM of a 152-SM part. A fixed rule, so
-// the workspace size does not depend on the device.
+// the largest that keeps the router grid within one wave of a 152-SM part (one CTA per SM: its
+// stage ring takes most of the shared memory). A fixed rule, so the workspace size does not
+// depend on the device.
+constexpr int kRouterWave = 152;
 int choose_ks(int T) {
   static const int opts[] = {44, 22, 11, 4, 2, 1};
   const int tiles = (T + kRouterN - 1) / kRouterN;
   for (int o : opts)
-    if (tiles * o <= 304) return o;
+    if (tiles * o <= kRouterWave) return o;
   return 1;
 }
-constexpr size_t kPartRowsSmall = 304 * kRouterN;  // max ks * T over the T where ks > 1
+constexpr size_t kPartRowsSmall = static_cast<size_t>(kRouterWave) * kRouterN;  // max ks * T where ks > 1
 
 // Tokens per warp of the top-k kernel: one (its expert counts go to 256-token chunks, so the
 // number of CTAs is not bounded).

@@ -64,7 +64,7 @@ __device__ __forceinline__ Cand warp_argmax(Cand c) {
 // logit with the 9th for the gap; renormalise, times per_expert_scale; slots listed in ascending
 // expert id. Each CTA counts its slots per expert; the last CTA to finish turns the counts into
 // expert offsets, per-CTA base positions and the grouped GEMMs' token-tile list.
-__global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers b) {
+__global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffers b) {
   __shared__ int hist_s[E];
   __shared__ int part_s[2][E];
   __shared__ int scan_s[E + 1];
@@ -80,17 +80,20 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
     const int t = blockIdx.x * tb + warp * p.tpw + i;
     if (t >= p.T) break;
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
-    uint4 xv[11];
     float ss = 0.0f;
+    {
+      uint4 xv[11];
 #pragma unroll
-    for (int c = 0; c < 11; ++c) {
-      xv[c] = xr[lane + 32 * c];
-      const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+      for (int c = 0; c < 11; ++c) xv[c] = xr[lane + 32 * c];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = bf16_lo(w4[j]), bb = bf16_hi(w4[j]);
-        ss = fmaf(a, a, ss);
-        ss = fmaf(bb, bb, ss);
+      for (int c = 0; c < 11; ++c) {
+        const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = bf16_lo(w4[j]), bb = bf16_hi(w4[j]);
+          ss = fmaf(a, a, ss);
+          ss = fmaf(bb, bb, ss);
+        }
       }
     }
     ss = warp_sum(ss);
@@ -102,8 +105,11 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
       uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
 #pragma unroll
       for (int c = 0; c < 11; ++c) {
+        // x again (an L1 hit: this warp read the row just above), so that the row does not stay in
+        // registers and the kernel keeps four CTAs per SM.
+        const uint4 xc = xr[lane + 32 * c];
         const int col = (lane + 32 * c) * 8;
-        const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+        const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
         const float4 a0 = *reinterpret_cast<const float4*>(p.pre_ff_ln + col);
         const float4 a1 = *reinterpret_cast<const float4*>(p.pre_ff_ln + col + 4);
         const float4 c0 = *reinterpret_cast<const float4*>(p.pre_ff_ln_2 + col);
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteParams p, Buffers 
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = xv[c];
+      for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = xr[lane + 32 * c];
     }
 
     // Logits: expert e = lane + 32 j, partial sums added in ascending split order.
@@ -372,39 +378,58 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteParams p, Buffe
 // in ascending expert id; in the full layer it is normalised by post_feedforward_layernorm_2, the
 // shared-MLP output by post_feedforward_layernorm_1, their sum by post_feedforward_layernorm, the
 // residual is added and the result multiplied by layer_scalar.
-__device__ __forceinline__ float block_sum(float v, float* red) {
+// Sum over the CTA of one or two values per thread; every thread gets the totals.
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum(v);
-  __syncthreads();
+  v.x = warp_sum(v.x);
+  v.y = warp_sum(v.y);
+  __syncthreads();  // red may still be read by the previous reduction
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  float s = 0.0f;
+  float2 s = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int w = 0; w < kCombineThreads / 32; ++w) s += red[w];
+  for (int w = 0; w < kCombineThreads / 32; ++w) {
+    s.x += red[w].x;
+    s.y += red[w].y;
+  }
   return s;
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p, Buffers b) {
-  __shared__ float red[kCombineThreads / 32];
-  __shared__ int pos_s[K];
+// One CTA per token, 8 features per thread. Every load that does not depend on another is issued
+// before the first use: the token's 8 slot positions, then its 8 rows of y, d and x, so the CTA
+// waits for memory about twice (positions, then rows) rather than once per load.
+__global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(CombineParams p, Buffers b) {
+  __shared__ float2 red[kCombineThreads / 32];
   const int t = blockIdx.x, tid = threadIdx.x;
   const int f = tid * 8;
   pdl_wait();
-  if (tid < K) {
-    int pos = b.slot_pos[static_cast<size_t>(t) * K + tid];
-    if (pos < 0 || pos >= p.T * K) {
-      atomicOr(b.status, kStatusBadIndex);
-      pos = 0;
-    }
-    pos_s[tid] = pos;
+  const int4 pa = *reinterpret_cast<const int4*>(b.slot_pos + static_cast<size_t>(t) * K);
+  const int4 pb = *reinterpret_cast<const int4*>(b.slot_pos + static_cast<size_t>(t) * K + 4);
+  float dv[8];
+  uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+  if (p.full_layer) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(b.d + static_cast<size_t>(t) * H + f));
+    const float4 c = __ldcs(reinterpret_cast<const float4*>(b.d + static_cast<size_t>(t) * H + f + 4));
+    dv[0] = a.x; dv[1] = a.y; dv[2] = a.z; dv[3] = a.w;
+    dv[4] = c.x; dv[5] = c.y; dv[6] = c.z; dv[7] = c.w;
+    xv = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + f);
   }
-  __syncthreads();
+  int pos[K] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+  const int n_slots = p.T * K;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if (pos[k] < 0 || pos[k] >= n_slots) {
+      if (tid == 0) atomicOr(b.status, kStatusBadIndex);
+      pos[k] = 0;
+    }
+  }
+  uint4 yv[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) yv[k] = __ldcs(reinterpret_cast<const uint4*>(b.y + static_cast<size_t>(pos[k]) * H + f));
+  // The 8 expert outputs in ascending expert id (the order of the token's slots).
   float moe[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) moe[j] = 0.0f;
-  uint4 yv[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) yv[k] = *reinterpret_cast<const uint4*>(b.y + static_cast<size_t>(pos_s[k]) * H + f);
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const uint32_t w4[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
@@ -419,41 +444,38 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
     o = make_uint4(pack_bf16(moe[0], moe[1]), pack_bf16(moe[2], moe[3]), pack_bf16(moe[4], moe[5]),
                    pack_bf16(moe[6], moe[7]));
   } else {
-    float dv[8];
-    {
-      const float* dr = b.d + static_cast<size_t>(t) * H + f;
-      const float4 a = *reinterpret_cast<const float4*>(dr);
-      const float4 c = *reinterpret_cast<const float4*>(dr + 4);
-      dv[0] = a.x; dv[1] = a.y; dv[2] = a.z; dv[3] = a.w;
-      dv[4] = c.x; dv[5] = c.y; dv[6] = c.z; dv[7] = c.w;
-    }
     float sd = 0.0f, sm = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       sd = fmaf(dv[j], dv[j], sd);
       sm = fmaf(moe[j], moe[j], sm);
     }
-    sd = block_sum(sd, red);
-    sm = block_sum(sm, red);
-    const float inv_d = 1.0f / sqrtf(sd / static_cast<float>(H) + p.eps);
-    const float inv_m = 1.0f / sqrtf(sm / static_cast<float>(H) + p.eps);
-    float s[8];
+    const float2 r = block_sum2(make_float2(sd, sm), red);
+    const float inv_d = 1.0f / sqrtf(r.x / static_cast<float>(H) + p.eps);
+    const float inv_m = 1.0f / sqrtf(r.y / static_cast<float>(H) + p.eps);
+    const float4 g1a = *reinterpret_cast<const float4*>(p.post_ff_ln_1 + f);
+    const float4 g1b = *reinterpret_cast<const float4*>(p.post_ff_ln_1 + f + 4);
+    const float4 g2a = *reinterpret_cast<const float4*>(p.post_ff_ln_2 + f);
+    const float4 g2b = *reinterpret_cast<const float4*>(p.post_ff_ln_2 + f + 4);
+    const float g1[8] = {g1a.x, g1a.y, g1a.z, g1a.w, g1b.x, g1b.y, g1b.z, g1b.w};
+    const float g2[8] = {g2a.x, g2a.y, g2a.z, g2a.w, g2b.x, g2b.y, g2b.z, g2b.w};
+    float sv[8];
     float ss = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      s[j] = dv[j] * inv_d * (1.0f + p.post_ff_ln_1[f + j]) + moe[j] * inv_m * (1.0f + p.post_ff_ln_2[f + j]);
-      ss = fmaf(s[j], s[j], ss);
+      sv[j] = dv[j] * inv_d * (1.0f + g1[j]) + moe[j] * inv_m * (1.0f + g2[j]);
+      ss = fmaf(sv[j], sv[j], ss);
     }
-    ss = block_sum(ss, red);
-    const float inv_s = 1.0f / sqrtf(ss / static_cast<float>(H) + p.eps);
-    const uint4 xv = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + f);
+    const float inv_s = 1.0f / sqrtf(block_sum2(make_float2(ss, 0.0f), red).x / static_cast<float>(H) + p.eps);
+    const float4 g3a = *reinterpret_cast<const float4*>(p.post_ff_ln + f);
+    const float4 g3b = *reinterpret_cast<const float4*>(p.post_ff_ln + f + 4);
+    const float g3[8] = {g3a.x, g3a.y, g3a.z, g3a.w, g3b.x, g3b.y, g3b.z, g3b.w};
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
     uint32_t ow[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float lo = (bf16_lo(xw[j]) + s[2 * j] * inv_s * (1.0f + p.post_ff_ln[f + 2 * j])) * p.layer_scalar;
-      const float hi =
-          (bf16_hi(xw[j]) + s[2 * j + 1] * inv_s * (1.0f + p.post_ff_ln[f + 2 * j + 1])) * p.layer_scalar;
+      const float lo = (bf16_lo(xw[j]) + sv[2 * j] * inv_s * (1.0f + g3[2 * j])) * p.layer_scalar;
+      const float hi = (bf16_hi(xw[j]) + sv[2 * j + 1] * inv_s * (1.0f + g3[2 * j + 1])) * p.layer_scalar;
       ow[j] = pack_bf16(lo, hi);
     }
     o = make_uint4(ow[0], ow[1], ow[2], ow[3]);

@@ -15,7 +15,7 @@
 //     64-wide chunk of h is summed on the tensor cores (3 parts x 64 products) into its own TMEM
 //     accumulator, and the chunk sums are added in fp32 registers, so the tensor core's own
 //     accumulation spans only the 192 products of one chunk.
-// MMA: M = 128 experts (A = a W' part, K-major, by TMA), N = 64 tokens (B = x rows, K-major,
+// MMA: M = 128 experts (A = a W' part, K-major, by TMA), N = 128 tokens (B = x rows, K-major,
 // staged by the producer warp). Warp 0 loads, warp 1 issues the MMAs, warps 2..5 add chunk sums.
 #include <cuda_bf16.h>
 
@@ -28,13 +28,20 @@ namespace {
 
 constexpr int kThreadsR = 192;
 constexpr int kTile = 128 * 64 * 2;              // one 128-row x 64-element bf16 tile, 16 KB
-constexpr int kBTile = kRouterN * 64 * 2;        // x tile, 8 KB
-constexpr int kStageR = 3 * kTile + kBTile;      // hi, mid, lo, x
 constexpr int kStagesR = 3;
 constexpr int kAccR = 4;                         // rotating chunk accumulators in TMEM
-constexpr int kSmemR = 1024 + kStagesR * kStageR + 256;
-constexpr uint32_t kIdescR = idesc_bf16_f32(128, kRouterN);
-static_assert(kBTile % 1024 == 0, "x tile alignment");
+
+// N = tokens per CTA: kRouterN, or 64 for decode-sized batches (a narrower MMA and epilogue).
+template <int N>
+struct RCfg {
+  static constexpr int kBTile = N * 64 * 2;      // x tile
+  static constexpr int kStage = 3 * kTile + kBTile;  // hi, mid, lo, x
+  static constexpr int kSmem = 1024 + kStagesR * kStage + 256;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(128, N);
+  static_assert(kBTile % 1024 == 0, "x tile alignment");
+  static_assert(kAccR * N <= 512, "TMEM columns");
+};
+constexpr int kRouterSmallN = 64;
 
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
@@ -85,11 +92,12 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+template <int N>
 __global__ void __launch_bounds__(kThreadsR, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap map_w, RouteParams p, Buffers b) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStagesR * kStageR);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStagesR * RCfg<N>::kStage);
   uint64_t* empty_bar = full_bar + kStagesR;
   uint64_t* accf_bar = empty_bar + kStagesR;
   uint64_t* acce_bar = accf_bar + kAccR;
@@ -97,7 +105,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kRouterN;
+  const int t0 = blockIdx.x * N;
   const int ks = blockIdx.y;
   const int cps = (H / 64) / p.ks;  // chunks per split
   const int c_begin = ks * cps;
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     prefetch_tmap(&map_w);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kAccR * kRouterN);
+    tmem_alloc(tmem_slot, kAccR * N);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       int got = 1;
       if (lane == 0) got = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty);
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
-      uint8_t* st = smem + stage * kStageR;
+      uint8_t* st = smem + stage * RCfg<N>::kStage;
       const int k0 = (c_begin + ci) * 64;
       if (lane == 0) {
         armed |= 1u << stage;
@@ -150,11 +158,11 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 #pragma unroll
         for (int part = 0; part < 3; ++part) tma_load_2d(st + part * kTile, &map_w, &full_bar[stage], k0, part * E, pol);
       }
-      // x rows t0..t0+63, 16-byte chunks copied asynchronously into the 128-byte-swizzled K-major
+      // x rows t0..t0+N-1, 16-byte chunks copied asynchronously into the 128-byte-swizzled K-major
       // tile (rows past T are zero-filled); each lane's arrival fires when its copies have landed.
       const uint32_t xs = smem_u32(st + 3 * kTile);
 #pragma unroll
-      for (int i = 0; i < (kRouterN * 8) / 32; ++i) {
+      for (int i = 0; i < (N * 8) / 32; ++i) {
         const int idx = lane + 32 * i, r = idx >> 3, cc = idx & 7;
         const int t = t0 + r;
         const uint16_t* src = p.x + static_cast<size_t>(t < p.T ? t : 0) * H + k0 + cc * 8;
@@ -181,14 +189,15 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, b.status, kStatusWaitFull)) break;
         fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + stage * kStageR);
+        const uint32_t sa = smem_u32(smem + stage * RCfg<N>::kStage);
         const uint64_t bdesc = smem_desc_sw128(sa + 3 * kTile);
-        const uint32_t d = tmem_base + acc * kRouterN;
+        const uint32_t d = tmem_base + acc * N;
 #pragma unroll
         for (int part = 0; part < 3; ++part) {
           const uint64_t adesc = smem_desc_sw128(sa + part * kTile);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdescR, (part | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, RCfg<N>::kIdesc, (part | k) != 0 ? 1u : 0u);
         }
         umma_commit(&empty_bar[stage]);
         umma_commit(&accf_bar[acc]);
@@ -208,9 +217,9 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   } else {
     // ---------------- warps 2..5: add the chunk sums (TMEM lane = expert) in fp32
     const int q = warp & 3;
-    float z[kRouterN];
+    float z[N];
 #pragma unroll
-    for (int j = 0; j < kRouterN; ++j) z[j] = 0.0f;
+    for (int j = 0; j < N; ++j) z[j] = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -223,9 +232,9 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int g = 0; g < kRouterN / 32; ++g) {
+      for (int g = 0; g < N / 32; ++g) {
         float v[32];
-        tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kRouterN + g * 32, v);
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * N + g * 32, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[g * 32 + j] += v[j];
       }
@@ -240,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     if (ok) {
       const int e = q * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < kRouterN; ++j) {
+      for (int j = 0; j < N; ++j) {
         const int t = t0 + j;
         if (t < p.T) b.logits_part[(static_cast<size_t>(ks) * p.T + t) * E + e] = z[j];
       }
@@ -252,14 +261,18 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   pdl_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kAccR * kRouterN);
+    tmem_dealloc(tmem_base, kAccR * N);
   }
 }
 
 }  // namespace
 
 cudaError_t router_set_smem_limit() {
-  return cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemR);
+  const cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<kRouterN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             RCfg<kRouterN>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_tc_kernel<kRouterSmallN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              RCfg<kRouterSmallN>::kSmem);
 }
 
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s) {
@@ -267,8 +280,12 @@ cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStrea
 }
 
 cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s) {
+  if (p.T <= kRouterSmallN)
+    return launch_pdl(router_tc_kernel<kRouterSmallN>, dim3(1, p.ks), dim3(kThreadsR),
+                      static_cast<size_t>(RCfg<kRouterSmallN>::kSmem), s, map_w, p, b);
   dim3 grid((p.T + kRouterN - 1) / kRouterN, p.ks);
-  return launch_pdl(router_tc_kernel, grid, dim3(kThreadsR), static_cast<size_t>(kSmemR), s, map_w, p, b);
+  return launch_pdl(router_tc_kernel<kRouterN>, grid, dim3(kThreadsR), static_cast<size_t>(RCfg<kRouterN>::kSmem), s,
+                    map_w, p, b);
 }
 
 }  // namespace moe
