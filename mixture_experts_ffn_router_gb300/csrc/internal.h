@@ -106,6 +106,27 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// The same for kernels that run as clusters of two CTAs (SM pairs); grid.x must be even.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 constexpr int kKernelsPerForward = 7;
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s);
@@ -120,6 +141,10 @@ cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int 
                         cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
 int gate_up_tiles_per_item(int bn, int T);
+// SM-pair (cta_group::2) down GEMM for token tiles of 256 (gemm_pair.cu).
+cudaError_t gemm_pair_set_smem_limits();
+int gemm_pair_max_clusters();
+cudaError_t launch_down_pair(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s);
 cudaError_t router_set_smem_limit();
 
 }  // namespace moe

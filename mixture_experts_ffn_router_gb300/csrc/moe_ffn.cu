@@ -154,6 +154,7 @@ struct moe_ffn_ctx {
   moe_ffn_config cfg;
   int device;
   int num_sms;
+  int pair_clusters;  // two-CTA clusters of the SM-pair GEMMs resident at once (0: do not use them)
   uint8_t* ws;
   size_t ws_bytes;
   Buffers buf;
@@ -208,13 +209,17 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
     return MOE_FFN_ECUDA;
   if (major != 10 || minor != 3) return MOE_FFN_EARCH;
   if (!get_encode()) return MOE_FFN_ECUDA;
-  if (gemm_set_smem_limits() != cudaSuccess || router_set_smem_limit() != cudaSuccess) return MOE_FFN_ECUDA;
+  if (gemm_set_smem_limits() != cudaSuccess || gemm_pair_set_smem_limits() != cudaSuccess ||
+      router_set_smem_limit() != cudaSuccess)
+    return MOE_FFN_ECUDA;
+  const int pair_clusters = gemm_pair_max_clusters();
 
   moe_ffn_ctx* c = new (std::nothrow) moe_ffn_ctx();
   if (!c) return MOE_FFN_ECUDA;
   c->cfg = *cfg;
   c->device = device;
   c->num_sms = sms;
+  c->pair_clusters = pair_clusters < sms / 2 ? pair_clusters : sms / 2;
   c->ws = static_cast<uint8_t*>(workspace);
   c->ws_bytes = workspace_bytes;
   uint8_t* w = c->ws;
@@ -381,7 +386,15 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
                         static_cast<long>(nd) * ((D / 64 + ma - 1) / ma);
   const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
   const int grid_gu = static_cast<int>(items_gu < c->num_sms ? items_gu : c->num_sms);
-  const int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
+  int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
+  // For token tiles of 256 (T above 1024) the down GEMM runs on SM pairs: M = 256 per pair of
+  // CTAs, half of each token tile in each CTA, so its B maps are the ones with 128-row boxes.
+  const bool pairs = bn == 256 && c->pair_clusters > 0;
+  if (pairs) {
+    grid_dn = 2 * c->pair_clusters;
+    dn.b_exp = c->map_h[2];
+    dn.b_dense = c->map_hd[2];
+  }
 
   cudaError_t e = cudaSuccess;
   for (int k = 0; k < kKernelsPerForward && e == cudaSuccess; ++k) {
@@ -393,7 +406,10 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4: e = launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s); break;
-      case 5: e = launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s); break;
+      case 5:
+        e = pairs ? launch_down_pair(dn, c->buf, T, rp.full_layer, grid_dn, s)
+                  : launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s);
+        break;
       case 6: e = launch_combine(cp, c->buf, s); break;
     }
     if (e == cudaSuccess && c->ev_stop[k]) e = cudaEventRecord(c->ev_stop[k], s);
