@@ -15,6 +15,8 @@ Pins (what the oracle is checked against, in ``tests/test_oracle_pins.py``):
   * The sparse == dense-masked identity of the 26B-A4B post ("The traceable trick"), bitwise.
   * The whole layer on tiny shapes against an independent float64 numpy brute force (brute.py).
   * The permutation against a brute-force sort of the slots by (expert, token).
+  * int8 experts: the quantiser's error bound, symmetry, exact rows and zero rows; the layer with
+    int8 experts against brute.py on the dequantised weights.
 """
 import ctypes
 
@@ -60,6 +62,10 @@ class Weights(ctypes.Structure):
         ("post_ff_ln_2", _f32p),
         ("post_ff_ln", _f32p),
         ("layer_scalar", ctypes.c_float),
+        ("gate_up_q", ctypes.POINTER(ctypes.c_int8)),
+        ("gate_up_scale", _f32p),
+        ("down_q", ctypes.POINTER(ctypes.c_int8)),
+        ("down_scale", _f32p),
     ]
 
 
@@ -99,6 +105,9 @@ def lib():
         L.moe_oracle_permute.restype = ctypes.c_int
         L.moe_oracle_permute.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _f32p,
                                          _i32p, _i32p, _i32p, _f32p, _i32p]
+        L.moe_oracle_quantize_int8.restype = ctypes.c_int
+        L.moe_oracle_quantize_int8.argtypes = [_u16p, ctypes.c_longlong, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_int8), _f32p]
         L.moe_oracle_set_threads.restype = None
         L.moe_oracle_set_threads.argtypes = [ctypes.c_int]
         L.moe_oracle_max_threads.restype = ctypes.c_int
@@ -178,6 +187,16 @@ def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked
             a = _as(a, np.uint16)
             keep[f] = a
             setattr(wst, f, _ptr(a, ctypes.c_uint16))
+    for f in ("gate_up_q", "down_q"):
+        a = weights.get(f)
+        if a is not None:
+            a = _as(a, np.int8)
+            keep[f] = a
+            setattr(wst, f, _ptr(a, ctypes.c_int8))
+            sc = _as(weights[f.replace("_q", "_scale")], np.float32)
+            keep[f.replace("_q", "_scale")] = sc
+            setattr(wst, f.replace("_q", "_scale"), _ptr(sc, ctypes.c_float))
+            keep.setdefault(f.replace("_q", ""), a)  # the bf16 form is not needed
     wst.layer_scalar = float(weights.get("layer_scalar", 1.0))
     if route_only:
         missing = [f for f in ("router_w", "router_norm_w", "per_expert_scale") if f not in keep]
@@ -216,6 +235,21 @@ def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked
     return res
 
 
+def quantize_int8(w_bf16: np.ndarray):
+    """Per-channel (per-row) symmetric int8 quantisation of a bf16 matrix (see
+    moe_oracle_quantize_int8). Returns (q int8 [rows, cols], scale float32 [rows])."""
+    w = _as(np.asarray(w_bf16), np.uint16)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    q = np.zeros(w.shape, np.int8)
+    scale = np.zeros(rows, np.float32)
+    rc = lib().moe_oracle_quantize_int8(_ptr(w, ctypes.c_uint16), rows, cols, _ptr(q, ctypes.c_int8),
+                                        _ptr(scale, ctypes.c_float))
+    if rc != 0:
+        raise ValueError("moe_oracle_quantize_int8: bad arguments")
+    return q, scale
+
+
 def permute(topk_idx: np.ndarray, topk_w, n_experts: int) -> dict:
     """Stable counting sort of the slots by expert (see moe_oracle_permute)."""
     idx = _as(np.asarray(topk_idx), np.int32)
@@ -242,5 +276,5 @@ def gemma_dims(full_layer: bool) -> dict:
             "full_layer": int(bool(full_layer)), "eps": 1e-6, "router_scale": 2816 ** -0.5}
 
 
-__all__ = ["lib", "gelu_tanh", "rmsnorm", "forward", "permute", "set_threads", "max_threads",
+__all__ = ["lib", "gelu_tanh", "rmsnorm", "forward", "permute", "quantize_int8", "set_threads", "max_threads",
            "gemma_dims", "Dims", "Weights", "Outputs"]

@@ -50,8 +50,10 @@ def forward(dims: dict, x_bits: np.ndarray, weights: dict) -> dict:
     psel = p[rows, top]
     M[rows, top] = psel / psel.sum(axis=1, keepdims=True) * f64("per_expert_scale")[top]
 
-    gu = bf16_to_f64(weights["gate_up"]).reshape(E, 2 * I, H)
-    dn = bf16_to_f64(weights["down"]).reshape(E, H, I)
+    # Expert weights: bf16 bits, or float64 values given as gate_up_f64 / down_f64 (for instance the
+    # dequantised int8 form of "Can it run on a smaller box?").
+    gu = (f64("gate_up_f64") if "gate_up_f64" in weights else bf16_to_f64(weights["gate_up"])).reshape(E, 2 * I, H)
+    dn = (f64("down_f64") if "down_f64" in weights else bf16_to_f64(weights["down"])).reshape(E, H, I)
     G = np.einsum("th,eih->tei", n2, gu[:, :I, :])
     U = np.einsum("th,eih->tei", n2, gu[:, I:, :])
     Y = np.einsum("tei,ehi->teh", _gelu(G) * U, dn)                 # every expert, every token

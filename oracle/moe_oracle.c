@@ -110,25 +110,34 @@ static void route_one(const moe_oracle_dims* d, const float* xin, const moe_orac
   }
 }
 
+/* Element (row, col) of an expert weight matrix with `cols` columns: the bf16 value, or, when the
+ * int8 form is given, q * scale of the row (exact in fp64: q has 8 bits, scale 24). */
+static double expert_weight(const uint16_t* bf, const int8_t* q, const float* scale, size_t row, size_t col,
+                            size_t cols) {
+  if (q) return (double)q[row * cols + col] * (double)scale[row];
+  return (double)bf16_to_f32(bf[row * cols + col]);
+}
+
 /* One expert's MLP on input v[H] ([MoE] "The architecture": fused gate_up [E,2I,H], down [E,H,I];
- * [Lab] gelu_pytorch_tanh): hvec = gelu_tanh(gate·v) * (up·v), y = down·hvec. */
+ * [Lab] gelu_pytorch_tanh): hvec = gelu_tanh(gate·v) * (up·v), y = down·hvec. With the int8 form
+ * ([MoE] "Can it run on a smaller box?": per-channel symmetric int8 experts) each weight is
+ * q * scale of its output row. */
 static void expert_mlp(const moe_oracle_dims* d, const moe_oracle_weights* w, int e,
                        const double* v, double* hvec, double* y) {
   const int H = d->hidden, I = d->moe_inter;
-  const uint16_t* gate = w->gate_up + (size_t)e * 2 * I * H;
-  const uint16_t* up = gate + (size_t)I * H;
+  const size_t g0 = (size_t)e * 2 * I;  /* first gate_up row of expert e */
   for (int i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     for (int h = 0; h < H; ++h) {
-      g += (double)bf16_to_f32(gate[(size_t)i * H + h]) * v[h];
-      u += (double)bf16_to_f32(up[(size_t)i * H + h]) * v[h];
+      g += expert_weight(w->gate_up, w->gate_up_q, w->gate_up_scale, g0 + i, h, H) * v[h];
+      u += expert_weight(w->gate_up, w->gate_up_q, w->gate_up_scale, g0 + I + i, h, H) * v[h];
     }
     hvec[i] = moe_oracle_gelu_tanh(g) * u;
   }
-  const uint16_t* down = w->down + (size_t)e * H * I;
+  const size_t d0 = (size_t)e * H;  /* first down row of expert e */
   for (int h = 0; h < H; ++h) {
     double acc = 0.0;
-    for (int i = 0; i < I; ++i) acc += (double)bf16_to_f32(down[(size_t)h * I + i]) * hvec[i];
+    for (int i = 0; i < I; ++i) acc += expert_weight(w->down, w->down_q, w->down_scale, d0 + h, i, I) * hvec[i];
     y[h] = acc;
   }
 }
@@ -165,6 +174,8 @@ static int dims_ok(const moe_oracle_dims* d) {
 int moe_oracle_forward(const moe_oracle_dims* d, int T, const uint16_t* x,
                        const moe_oracle_weights* w, const moe_oracle_outputs* o, int masked_dense) {
   if (!dims_ok(d) || T < 0 || !w || !o || (T > 0 && !x)) return -1;
+  if ((!w->gate_up && !(w->gate_up_q && w->gate_up_scale)) || (!w->down && !(w->down_q && w->down_scale)))
+    return -1;
   const int H = d->hidden, E = d->n_experts, K = d->top_k, I = d->moe_inter;
   const int D = d->full_layer ? d->dense_inter : 1;
   int bad = 0;
@@ -314,6 +325,30 @@ int moe_oracle_route(const moe_oracle_dims* d, int T, const uint16_t* x, const m
 
 /* Slots sorted by (expert, token): the gather that precedes each expert's MLP and the scatter
  * back ([MoE] "The architecture": the experts' sparse gather/scatter loop), as a counting sort. */
+int moe_oracle_quantize_int8(const uint16_t* w, long long rows, int cols, int8_t* q, float* scale) {
+  if (!w || !q || !scale || rows < 0 || cols < 1) return -1;
+  for (long long r = 0; r < rows; ++r) {
+    const uint16_t* wr = w + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int c = 0; c < cols; ++c) {
+      const float a = fabsf(bf16_to_f32(wr[c]));
+      if (a > amax) amax = a;
+    }
+    const float s = amax / 127.0f;
+    scale[r] = s;
+    for (int c = 0; c < cols; ++c) {
+      float v = 0.0f;
+      if (s > 0.0f) {
+        v = rintf(bf16_to_f32(wr[c]) / s);
+        if (v > 127.0f) v = 127.0f;
+        if (v < -127.0f) v = -127.0f;
+      }
+      q[(size_t)r * cols + c] = (int8_t)v;
+    }
+  }
+  return 0;
+}
+
 int moe_oracle_permute(int T, int K, int E, const int32_t* topk_idx, const float* topk_w,
                        int32_t* counts, int32_t* offsets, int32_t* perm, float* w_sorted,
                        int32_t* slot_pos) {

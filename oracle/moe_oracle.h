@@ -61,6 +61,13 @@ typedef struct moe_oracle_weights {
   const float* post_ff_ln_2;      /* [H] */
   const float* post_ff_ln;        /* [H] */
   float layer_scalar;
+  /* Optional int8 form of the expert weights ([MoE] "Can it run on a smaller box?": per-channel
+   * symmetric int8 experts). When gate_up_q is set, expert weight (row, col) of gate_up is
+   * gate_up_q[row, col] * gate_up_scale[row] and gate_up may be NULL; likewise for down. */
+  const int8_t* gate_up_q;        /* [E * 2I, H] */
+  const float* gate_up_scale;     /* [E * 2I] */
+  const int8_t* down_q;           /* [E * H, I] */
+  const float* down_scale;        /* [E * H] */
 } moe_oracle_weights;
 
 /* Every field may be NULL (not written). Slot (t, k): token t's k-th selected expert, k in
@@ -97,6 +104,12 @@ int moe_oracle_forward(const moe_oracle_dims* d, int T, const uint16_t* x,
  * Returns 0, or -1 on bad arguments. */
 int moe_oracle_route(const moe_oracle_dims* d, int T, const uint16_t* x, const moe_oracle_weights* w,
                      const moe_oracle_outputs* o);
+
+/* Per-channel symmetric int8 quantisation of a bf16 matrix [rows, cols] (one channel per row):
+ * scale[r] = max_c |w[r, c]| / 127 (fp32), q[r, c] = w[r, c] / scale[r] (fp32) rounded to nearest,
+ * ties to even, clamped to [-127, 127]; an all-zero row gets scale 0 and q 0. Returns 0, or -1 on
+ * bad arguments. */
+int moe_oracle_quantize_int8(const uint16_t* w, long long rows, int cols, int8_t* q, float* scale);
 
 /* Stable counting sort of the T*K slots by expert: counts[E], offsets[E+1] (exclusive prefix sum,
  * offsets[E] = T*K), perm[T*K] (token of each sorted slot; within one expert tokens ascend),
