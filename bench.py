@@ -43,6 +43,9 @@ WORKLOADS = {
                      desc="Gemma-4 26B-A4B full dual-path FFN layer, decode batch T=64, uniform routing"),
     "prefill4096": dict(full=True, T=4096, skew=True,
                         desc="Gemma-4 26B-A4B full dual-path FFN layer, prefill T=4096, Zipf(1.1)-scaled router rows"),
+    "decode64_int8": dict(full=True, T=64, skew=False, int8=True,
+                          desc="Gemma-4 26B-A4B full dual-path FFN layer, decode batch T=64, uniform routing, "
+                               "int8 per-channel experts"),
     "moe8": dict(full=False, T=8, skew=False, desc="Gemma-4 26B-A4B MoE block only (router + experts), T=8"),
     "layer": dict(full=True, T=None, skew=False, desc="Gemma-4 26B-A4B full dual-path FFN layer, uniform routing"),
     "stack30": dict(full=True, T=256, skew=False, layers=30,
@@ -234,6 +237,10 @@ def run_reference(args, wl):
     T = wl["T"]
     n = min(T, 64)
     w = synth.host_arrays(synth.make_weights(seed=args.seed, device="cpu", full_layer=wl["full"], skew=wl["skew"]))
+    if wl.get("int8"):
+        for name, cols in (("gate_up", H), ("down", I)):
+            q, sc = oracle.quantize_int8(w.pop(name).reshape(-1, cols))
+            w[name + "_q"], w[name + "_scale"] = q, sc
     x = synth.bf16_bits(synth.make_x(T, seed=args.seed, device="cpu"))[:n]
     dims = oracle.gemma_dims(wl["full"])
     for _ in range(max(args.warmup, 0)):
@@ -276,6 +283,12 @@ def run_ours(args, wl):
     # One context per layer, all sharing the first one's workspace (their forwards never overlap).
     weights = [synth.make_weights(seed=args.seed, layer=l, device=dev, full_layer=wl["full"], skew=wl["skew"])
                for l in range(L)]
+    if wl.get("int8"):
+        # int8 experts, made on the device; the bf16 experts are then dropped.
+        weights = [B.quantize_experts_int8(w) for w in weights]
+        torch.cuda.synchronize()
+        for w in weights:
+            del w["gate_up"], w["down"]
     x = synth.make_x(T, seed=args.seed, device=dev)
     bufs = [torch.empty_like(x), torch.empty_like(x)]
     ctxs = [B.MoeFFN(mode, T, device=local)]
@@ -380,10 +393,13 @@ def run_ours(args, wl):
     hbm, tc_burst, tc_sus, peak_src = measured_peaks()
     S = T * K
     full = wl["full"]
-    gu_bytes = experts_hit * GATE_UP_BYTES_PER_EXPERT + (DENSE_GATE_UP_BYTES if full else 0) \
+    # int8 experts: one byte per weight plus a 4-byte scale per row.
+    gu_pe = (2 * I * H + 2 * I * 4) if wl.get("int8") else GATE_UP_BYTES_PER_EXPERT
+    dn_pe = (H * I + H * 4) if wl.get("int8") else DOWN_BYTES_PER_EXPERT
+    gu_bytes = experts_hit * gu_pe + (DENSE_GATE_UP_BYTES if full else 0) \
         + T * H * 2 * (2 if full else 1) + S * I * 2 + (T * D * 2 if full else 0)
     gu_flops = 2 * S * 2 * I * H + (2 * T * 2 * D * H if full else 0)
-    dn_bytes = experts_hit * DOWN_BYTES_PER_EXPERT + (DENSE_DOWN_BYTES if full else 0) \
+    dn_bytes = experts_hit * dn_pe + (DENSE_DOWN_BYTES if full else 0) \
         + S * I * 2 + (T * D * 2 if full else 0) + S * H * 2 + (T * H * 4 if full else 0)
     dn_flops = 2 * S * H * I + (2 * T * H * D if full else 0)
     per_kernel = {"gate_up_gemm": (gu_bytes, gu_flops), "down_gemm": (dn_bytes, dn_flops)}
@@ -399,7 +415,7 @@ def run_ours(args, wl):
     roof["algorithmic_bytes"] = kb
     roof["algorithmic_flops"] = kf
     roof["peak_source"] = peak_src
-    layer_bytes = experts_hit * (GATE_UP_BYTES_PER_EXPERT + DOWN_BYTES_PER_EXPERT) + ROUTER_BYTES + T * H * 2 * 2 \
+    layer_bytes = experts_hit * (gu_pe + dn_pe) + ROUTER_BYTES + T * H * 2 * 2 \
         + ((DENSE_GATE_UP_BYTES + DENSE_DOWN_BYTES) if full else 0)
     layer_flops = T * (FLOPS_PER_TOKEN_EXPERTS + (FLOPS_PER_TOKEN_DENSE if full else 0))
     t_roof = max(layer_bytes / (hbm * 1e9), layer_flops / (tc_burst * 1e12))
@@ -447,6 +463,7 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl["desc"], "T": T, "tokens_per_gpu": T, "hidden": H, "experts": E, "top_k": K,
                        "moe_inter": I, "dense_inter": D if wl["full"] else 0,
+                       "expert_weights": "int8, per-row fp32 scale" if wl.get("int8") else "bf16",
                        "layers": L,
                        "l2": "inputs larger than L2 (%.2f GB of weights read per step)" % (layer_bytes * L / 1e9),
                        "parallelism": "replicas (dp%d, no collective)" % world},

@@ -93,6 +93,14 @@ typedef struct moe_ffn_weights {
   const float* post_ff_ln_2;      /* [2816] fp32: post_feedforward_layernorm_2 (expert branch output) */
   const float* post_ff_ln;        /* [2816] fp32: post_feedforward_layernorm (after the sum) */
   float layer_scalar;             /* required; multiplies (residual + normed sum) */
+  /* Optional int8 experts ("Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS Inferentia2",
+   * section "Can it run on a smaller box?": per-channel symmetric int8). When gate_up_q is not
+   * NULL, all four fields must be set; the experts' weights are then q[row, col] * scale[row] and
+   * gate_up / down are not read (the shared MLP stays bf16). moe_ffn_quantize_int8 makes them. */
+  const int8_t* gate_up_q;        /* [128 * 1408, 2816] int8 */
+  const float* gate_up_scale;     /* [128 * 1408] fp32, one per row */
+  const int8_t* down_q;           /* [128 * 2816, 704] int8 */
+  const float* down_scale;        /* [128 * 2816] fp32, one per row */
 } moe_ffn_weights;
 
 /* Device views into the workspace, filled by moe_ffn_workspace_view. Contents are those of the
@@ -182,6 +190,14 @@ int moe_ffn_router_logits_noalloc(const void* x, int T, const float* router_w, c
                                   float router_scale, float eps, float* logits, void* stream);
 
 /* A static string naming a status code. */
+/* Per-channel symmetric int8 quantisation of a bf16 matrix [rows, cols] on the device, one channel
+ * per row: scale[r] = max_c |w[r, c]| / 127 in fp32, q[r, c] = w[r, c] / scale[r] in fp32 rounded
+ * to nearest (ties to even) and clamped to [-127, 127]; an all-zero row gets scale 0 and q 0. All
+ * pointers are device pointers; w and q 16-byte aligned, cols a multiple of 8. Asynchronous on
+ * `stream`. Returns MOE_FFN_EINVAL / MOE_FFN_EALIGN on bad arguments, MOE_FFN_ECUDA if the launch
+ * fails. */
+int moe_ffn_quantize_int8(const void* w, long long rows, int cols, int8_t* q, float* scale, void* stream);
+
 const char* moe_ffn_status_string(int status);
 
 /* Releases the host state of a context (it holds no device memory). Never frees the workspace or

@@ -36,8 +36,11 @@ WEIGHT_FIELDS = ("router_w", "router_norm_w", "per_expert_scale", "gate_up", "do
                  "dense_down", "pre_ff_ln", "pre_ff_ln_2", "post_ff_ln_1", "post_ff_ln_2", "post_ff_ln")
 
 
+INT8_FIELDS = ("gate_up_q", "gate_up_scale", "down_q", "down_scale")
+
+
 class moe_ffn_weights(ctypes.Structure):
-    _fields_ = [(f, _vp) for f in WEIGHT_FIELDS] + [("layer_scalar", ctypes.c_float)]
+    _fields_ = [(f, _vp) for f in WEIGHT_FIELDS] + [("layer_scalar", ctypes.c_float)] + [(f, _vp) for f in INT8_FIELDS]
 
 
 VIEW_FIELDS = ("logits", "topk_idx", "topk_w", "gap", "counts", "offsets", "perm", "w_sorted", "slot_pos", "n1",
@@ -79,6 +82,8 @@ def lib():
                                                      _vp, _vp]
         L.moe_ffn_status_string.restype = ctypes.c_char_p
         L.moe_ffn_status_string.argtypes = [ctypes.c_int]
+        L.moe_ffn_quantize_int8.restype = ctypes.c_int
+        L.moe_ffn_quantize_int8.argtypes = [_vp, ctypes.c_longlong, ctypes.c_int, _vp, _vp, _vp]
         L.moe_ffn_destroy.restype = None
         L.moe_ffn_destroy.argtypes = [_vp]
         _LIB = L
@@ -152,6 +157,26 @@ def moe_ffn_router_logits_noalloc(x: int, T: int, router_w: int, router_norm_w: 
                                                float(router_scale), float(eps), _vp(logits), _vp(stream))
 
 
+def moe_ffn_quantize_int8(w: int, rows: int, cols: int, q: int, scale: int, stream: int) -> int:
+    return lib().moe_ffn_quantize_int8(_vp(w), int(rows), int(cols), _vp(q), _vp(scale), _vp(stream))
+
+
+def quantize_experts_int8(w: dict) -> dict:
+    """Adds the int8 form of the experts (gate_up_q/scale, down_q/scale) to a dict of CUDA weight
+    tensors, made on the device by moe_ffn_quantize_int8."""
+    import torch
+    out = dict(w)
+    s = torch.cuda.current_stream().cuda_stream
+    for name, rows, cols in (("gate_up", N_EXPERTS * 2 * MOE_INTER, HIDDEN), ("down", N_EXPERTS * HIDDEN, MOE_INTER)):
+        src = w[name]
+        q = torch.empty((rows, cols), dtype=torch.int8, device=src.device)
+        sc = torch.empty(rows, dtype=torch.float32, device=src.device)
+        _check("moe_ffn_quantize_int8", moe_ffn_quantize_int8(src.data_ptr(), rows, cols, q.data_ptr(), sc.data_ptr(), s))
+        out[name + "_q"] = q
+        out[name + "_scale"] = sc
+    return out
+
+
 def moe_ffn_destroy(ctx: int) -> None:
     lib().moe_ffn_destroy(_vp(ctx))
 
@@ -161,7 +186,7 @@ def moe_ffn_destroy(ctx: int) -> None:
 def weights_struct(w: dict) -> moe_ffn_weights:
     """A moe_ffn_weights whose fields point at the CUDA tensors of ``w`` (absent fields are NULL)."""
     s = moe_ffn_weights()
-    for f in WEIGHT_FIELDS:
+    for f in WEIGHT_FIELDS + INT8_FIELDS:
         t = w.get(f)
         if t is not None:
             if not t.is_cuda or not t.is_contiguous():

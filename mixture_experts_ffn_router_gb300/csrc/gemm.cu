@@ -51,20 +51,32 @@ constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 // MA = weight tiles per work item: 1, or 2 (an M = 256 item: two 128-row weight tiles share each
 // K chunk of the token tile, which cuts the operand bytes per FLOP from (1/128 + 1/BN) to
 // (1/256 + 1/BN) of the row bytes).
-template <int BN, bool GATE_UP, int MA>
+//
+// Q8: the experts' weights are int8 with one scale per row. A producer warp streams them by TMA into
+// a ring of their own (kRawSlots slots of two K chunks: 128-byte rows, 128-byte swizzle), four
+// converter warps widen each chunk into the bf16 A tile of a stage (one K chunk per stage, in the
+// 128-byte swizzled layout TMA would write), and the epilogue multiplies the accumulator by the
+// row's scale.
+template <int BN, bool GATE_UP, int MA, bool Q8 = false>
 struct Cfg {
-  static constexpr int KC = BN <= 64 ? 2 : 1;
+  static constexpr int KC = (BN <= 64 && !Q8) ? 2 : 1;
   static constexpr int kAStage = MA * kAChunk;                     // A bytes of one K chunk
   static constexpr int kBChunk = BN * kBK * 2;
   static constexpr int kChunkBytes = kAStage + kBChunk;
   static constexpr int kStageBytes = KC * kChunkBytes;
-  static constexpr int kStagesRaw = kRingBudget / kStageBytes;
+  static constexpr int kRawSlots = Q8 ? 6 : 0;                     // int8 weight ring
+  static constexpr int kRawSlotBytes = 2 * kBM * kBK;              // two K chunks of 128 int8 rows
+  static constexpr int kStagesRaw = (kRingBudget - kRawSlots * kRawSlotBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kEpiWarps = 4 * MA;                         // one per TMEM lane quarter and tile
   static constexpr int kGatherWarps = GATE_UP ? 4 : 0;
   static constexpr int kGatherWarp0 = 2 + kEpiWarps;
-  static constexpr int kThreads = (2 + kEpiWarps + kGatherWarps) * 32;
-  static constexpr int kFullArrivals = 1 + kGatherWarps * 32;
+  static constexpr int kConvWarps = Q8 ? 8 : 0;                    // int8 -> bf16 converters
+  static constexpr int kConvWarp0 = kGatherWarp0 + kGatherWarps;
+  static constexpr int kRawWarp = kConvWarp0 + kConvWarps;         // the int8 producer (Q8)
+  static constexpr int kThreads = (kRawWarp + (Q8 ? 1 : 0)) * 32;
+  static constexpr int kFullArrivals = 1 + kGatherWarps * 32 + kConvWarps;
+  static constexpr int kItemConsumers = 1 + kEpiWarps + kGatherWarps + kConvWarps + (Q8 ? 1 : 0);
   static constexpr int kAccCols = MA * BN;                         // TMEM columns of one accumulator set
   static constexpr int kNAcc = 2 * kAccCols <= 512 ? 2 : 1;        // double-buffered where it fits
   static constexpr int kTmemColsRaw = kNAcc * kAccCols;
@@ -78,12 +90,14 @@ struct Cfg {
   // gate_up: the gate/up hand-over [warps][16][32] fp32; down: a 32x32 output chunk per warp.
   static constexpr int kXchgBytes = kEpiWarps * (GATE_UP ? 16 * 32 * 4 : 32 * 32 * 4);
   static constexpr int kBarBytes = 512;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kXchgBytes + kBarBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kRawSlots * kRawSlotBytes + kXchgBytes + kBarBytes;
   static_assert(kChunkBytes % 1024 == 0, "operand tiles must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
   static_assert(MA == 1 || MA == 2, "MA");
   static_assert(kTmemColsRaw <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(kStages >= 2, "stages");
+  static_assert(!Q8 || (MA == 1 && KC == 1), "int8 weights: one weight tile per item, one K chunk per stage");
+  static_assert(!Q8 || 128 % (8 * kConvWarps) == 0, "converter rows");
   static_assert(kSmem <= 231424, "shared memory");
 };
 
@@ -199,24 +213,29 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
-template <int BN, bool GATE_UP, int MA>
-__global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
+template <int BN, bool GATE_UP, int MA, bool Q8>
+__global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a_exp, const __grid_constant__ CUtensorMap map_a_d0,
                         const __grid_constant__ CUtensorMap map_a_d1, const __grid_constant__ CUtensorMap map_b_exp,
-                        const __grid_constant__ CUtensorMap map_b_dense, Buffers b, int T, int full_layer) {
-  using C = Cfg<BN, GATE_UP, MA>;
+                        const __grid_constant__ CUtensorMap map_b_dense, Buffers b, int T, int full_layer,
+                        const __grid_constant__ CUtensorMap map_q, const float* q_scale) {
+  using C = Cfg<BN, GATE_UP, MA, Q8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kXchgBytes);
+  uint8_t* raw_ring = smem + C::kStages * C::kStageBytes;  // Q8: int8 weight slots
+  uint8_t* after_rings = raw_ring + C::kRawSlots * C::kRawSlotBytes;
+  float* xchg = reinterpret_cast<float*>(after_rings);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(after_rings + C::kXchgBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
   uint64_t* accf_bar = empty_bar + C::kStages;  // [kNAcc] accumulator ready
   uint64_t* acce_bar = accf_bar + 2;            // [kNAcc] accumulator drained
   uint64_t* final_bar = acce_bar + 2;
   uint64_t* itemf_bar = final_bar + 1;          // [kItemSlots] item published
   uint64_t* iteme_bar = itemf_bar + kItemSlots; // [kItemSlots] item read by every consumer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(iteme_bar + kItemSlots);
+  uint64_t* rawf_bar = iteme_bar + kItemSlots;  // [6] Q8: an int8 slot has landed
+  uint64_t* rawe_bar = rawf_bar + 6;            // [6] Q8: the converters are done with a slot
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rawe_bar + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* width_s = reinterpret_cast<int*>(tmem_slot + 2);  // [kStages] MMA width of each stage
   volatile int* item_s = reinterpret_cast<volatile int*>(width_s + 8);  // [kItemSlots] item ring
@@ -235,12 +254,17 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
     mbar_init(final_bar, 1);
     for (int k = 0; k < kItemSlots; ++k) {
       mbar_init(&itemf_bar[k], 1);
-      mbar_init(&iteme_bar[k], 1 + C::kEpiWarps + C::kGatherWarps);
+      mbar_init(&iteme_bar[k], C::kItemConsumers);
+    }
+    for (int r = 0; r < C::kRawSlots; ++r) {
+      mbar_init(&rawf_bar[r], 1);
+      mbar_init(&rawe_bar[r], C::kConvWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&map_a_exp);
     if (!GATE_UP) prefetch_tmap(&map_b_exp);
+    if (Q8) prefetch_tmap(&map_q);
     if (full_layer) {
       prefetch_tmap(&map_a_d0);
       if (GATE_UP) prefetch_tmap(&map_a_d1);
@@ -314,6 +338,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
       // gate_up with two tiles: tile 0 holds the gate rows and tile 1 the up rows of 128 features
       // ("paired"); otherwise each tile holds the gate and up rows of 64 features ("stacked").
       const bool paired = GATE_UP && MA == 2 && na == 2;
+      // Q8: the experts' A tiles are written by the converter warps, not by TMA.
+      const bool a_tma = !(Q8 && !it.dense);
       for (int c0 = 0; c0 < nch; c0 += C::KC) {
         if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
@@ -329,7 +355,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           width_s[stage] = width | (na << 16);
-          mbar_arrive_expect_tx(&full_bar[stage], nck * (na * kAChunk + (b_tma ? C::kBChunk : 0)));
+          mbar_arrive_expect_tx(&full_bar[stage], nck * ((a_tma ? na * kAChunk : 0) + (b_tma ? C::kBChunk : 0)));
           for (int cc = 0; cc < nck; ++cc) {
             uint8_t* a_dst = st + cc * C::kChunkBytes;
             const int k0 = (c0 + cc) * kBK;
@@ -344,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
               tma_load_2d(a_dst + kAChunk, mu, &full_bar[stage], k0, urow, pol_w);
               tma_load_2d(a_dst + kAChunk + kAChunk / 2, mu, &full_bar[stage], k0, urow + 64, pol_w);
             }
-            for (int a = 0; a < (paired ? 0 : na); ++a) {
+            for (int a = 0; a < (paired || !a_tma ? 0 : na); ++a) {
               const int tile = it.m * MA + a;
               if (GATE_UP) {
                 const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
@@ -403,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
           }
           // The gathered B rows were written by cp.async (generic proxy); the MMA reads them through
           // the async proxy.
-          if (GATE_UP) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          if (GATE_UP || Q8) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after();
           // The MMA is only as wide as the tile's token rows (rounded up to the MMA's step of 16).
           if (c0 == 0) {
@@ -495,11 +521,22 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
       }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * C::kAccCols + ta * BN);
+      // Q8: this lane's weight row's scale (gate_up: lanes 0..63 gate rows, 64..127 up rows).
+      float row_scale = 1.0f;
+      if (Q8 && !it.dense && has_tile) {
+        const size_t row = GATE_UP ? static_cast<size_t>(it.e) * (2 * I) + (q < 2 ? 0 : I) + tile * 64 + 32 * (q & 1) + lane
+                                   : static_cast<size_t>(it.e) * H + tile * kBM + 32 * q + lane;
+        row_scale = __ldg(q_scale + row);
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         if (paired || !has_tile || c * 32 >= it.rows) break;
         float v[32];
         tmem_ld32(t_row + c * 32, v);
+        if (Q8) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= row_scale;
+        }
         if (GATE_UP) {
           // q 0/1: gate of features f0+32(q&1)+lane; q 2/3: up of the same features.
           const bool gate_holder = q < 2;
@@ -586,7 +623,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
         acc_phase ^= 1u;
       }
     }
-  } else {
+  } else if (warp < C::kConvWarp0) {
     // ---------------- gather warps (gate_up only): expert token rows of n2 by cp.async
     const int g = threadIdx.x - C::kGatherWarp0 * 32;  // 0..127
     const int chunk16 = g & 7;               // which 16 bytes of the 128-byte row
@@ -644,6 +681,127 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
       }
     }
     cp_async_wait_all();
+  } else if (warp < C::kRawWarp) {
+    // ---------------- converters (Q8): chunk h of an int8 slot (K chunks 2j and 2j + 1 of 128 weight
+    // rows) becomes the bf16 A tile of the stage of K chunk 2j + h. Lane l reads 16 bytes (piece
+    // l % 4 of the chunk's 64) of row 8 * step + l / 4 of its warp's 16 rows; with the swizzle the
+    // eight rows of one instruction fall on different banks.
+    const int cw = warp - C::kConvWarp0;
+    const int pl = lane & 3;
+    int stage = 0, r = 0;
+    uint32_t phase = 0, rphase = 0;
+    bool ok = true;
+    int slot = 0;
+    uint32_t slot_par = 0;
+    while (ok) {
+      const int i = warp_next_item(itemf_bar, iteme_bar, item_s, slot, slot_par, abort_flag, b.status);
+      if (i < 0) break;
+      const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+      const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
+      for (int c0 = 0; c0 < nch; ++c0) {
+        if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
+          ok = false;
+          break;
+        }
+        if (!it.dense) {
+          const int h = c0 & 1;
+          if (h == 0 && !warp_wait(&rawf_bar[r], rphase, abort_flag, b.status, kStatusWaitFull)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* raw = raw_ring + r * C::kRawSlotBytes;
+          uint8_t* st = stages + stage * C::kStageBytes;
+#pragma unroll
+          for (int step = 0; step < 128 / (8 * C::kConvWarps); ++step) {
+            const int row = cw * (128 / C::kConvWarps) + step * 8 + (lane >> 2);
+            const int sw = row & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * 128 + (((4 * h + pl) ^ sw) << 4));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint8_t* row_dst = st + row * 128;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t o[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                // Bytes 2(j & 1) and 2(j & 1) + 1 of the word, widened exactly: with u = q + 128
+                // (the byte with its top bit flipped), the fp32 word 0x4B000000 | u is 2^23 + u, so
+                // subtracting 2^23 + 128 gives q; |q| < 256 leaves the low 16 bits zero, so the high
+                // halves are the bf16 values.
+                const uint32_t wx = w4[hh * 2 + (j >> 1)] ^ 0x80808080u;
+                const uint32_t k0 = (j & 1) * 2;
+                const float q0 = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | k0)) - 8388736.0f;
+                const float q1 = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | (k0 + 1))) - 8388736.0f;
+                o[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632u);
+              }
+              const int piece = 2 * pl + hh;
+              *reinterpret_cast<uint4*>(row_dst + ((piece ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          // The tile was written through the generic proxy; the MMA reads it through the async proxy.
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (h == 1 || c0 + 1 == nch) {
+            if (lane == 0) mbar_arrive(&rawe_bar[r]);
+            if (++r == C::kRawSlots) {
+              r = 0;
+              rphase ^= 1u;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_bar[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---------------- int8 producer (Q8): the experts' int8 weight rows, two K chunks per slot
+    const uint64_t pol_once = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    int r = 0;
+    uint32_t rphase = 0;
+    uint32_t armed = 0, armed_par = 0;
+    bool ok = true;
+    int slot = 0;
+    uint32_t slot_par = 0;
+    while (ok) {
+      const int i = warp_next_item(itemf_bar, iteme_bar, item_s, slot, slot_par, abort_flag, b.status);
+      if (i < 0) break;
+      const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+      if (it.dense) continue;
+      const uint64_t pol = it.nt > 2 ? pol_keep : pol_once;
+      for (int c0 = 0; c0 < C::kChunksExp; c0 += 2) {
+        if (!warp_wait(&rawe_bar[r], rphase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          armed |= 1u << r;
+          armed_par = (armed_par & ~(1u << r)) | (rphase << r);
+          mbar_arrive_expect_tx(&rawf_bar[r], C::kRawSlotBytes);
+          uint8_t* dst = raw_ring + r * C::kRawSlotBytes;
+          const int x0 = c0 * kBK;  // int8: one byte per element
+          if (GATE_UP) {
+            tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + it.m * 64, pol);
+            tma_load_2d(dst + 64 * 128, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + I + it.m * 64, pol);
+          } else {
+            tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * H + it.m * kBM, pol);
+          }
+        }
+        __syncwarp();
+        if (++r == C::kRawSlots) {
+          r = 0;
+          rphase ^= 1u;
+        }
+      }
+    }
+    // Every load issued above must have landed before the CTA exits.
+    if (lane == 0)
+      for (int s2 = 0; s2 < C::kRawSlots; ++s2)
+        if (armed & (1u << s2)) mbar_wait_timeout(&rawf_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs, b.status);
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -655,18 +813,18 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA>::kThreads, 1)
   }
 }
 
-template <int BN, bool GATE_UP, int MA>
+template <int BN, bool GATE_UP, int MA, bool Q8 = false>
 cudaError_t launch_t(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s) {
-  using C = Cfg<BN, GATE_UP, MA>;
-  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP, MA>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
-                    m.a_dense0, m.a_dense1, m.b_exp, m.b_dense, b, T, full_layer);
+  using C = Cfg<BN, GATE_UP, MA, Q8>;
+  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP, MA, Q8>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
+                    m.a_dense0, m.a_dense1, m.b_exp, m.b_dense, b, T, full_layer, m.a_q, m.q_scale);
 }
 
-template <int BN, bool GATE_UP, int MA>
+template <int BN, bool GATE_UP, int MA, bool Q8 = false>
 cudaError_t set_limit() {
-  using C = Cfg<BN, GATE_UP, MA>;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GATE_UP, MA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              C::kSmem);
+  using C = Cfg<BN, GATE_UP, MA, Q8>;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GATE_UP, MA, Q8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
 }
 
 }  // namespace
@@ -688,7 +846,30 @@ cudaError_t gemm_set_smem_limits() {
   if ((e = set_limit<32, false, 1>()) != cudaSuccess) return e;
   if ((e = set_limit<64, false, 1>()) != cudaSuccess) return e;
   if ((e = set_limit<128, false, 1>()) != cudaSuccess) return e;
-  return set_limit<256, false, 1>();
+  if ((e = set_limit<256, false, 1>()) != cudaSuccess) return e;
+  if ((e = set_limit<32, true, 1, true>()) != cudaSuccess) return e;
+  if ((e = set_limit<64, true, 1, true>()) != cudaSuccess) return e;
+  if ((e = set_limit<32, false, 1, true>()) != cudaSuccess) return e;
+  return set_limit<64, false, 1, true>();
+}
+
+// int8 experts (token tiles of 32 or 64): m.a_q is the int8 expert map, m.q_scale the row scales.
+cudaError_t launch_gate_up_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+                              cudaStream_t s) {
+  switch (bn) {
+    case 32: return launch_t<32, true, 1, true>(m, b, T, full_layer, grid, s);
+    case 64: return launch_t<64, true, 1, true>(m, b, T, full_layer, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_down_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+                           cudaStream_t s) {
+  switch (bn) {
+    case 32: return launch_t<32, false, 1, true>(m, b, T, full_layer, grid, s);
+    case 64: return launch_t<64, false, 1, true>(m, b, T, full_layer, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,

@@ -85,6 +85,8 @@ struct CombineParams {
 // down: a_exp = down rows, a_dense0 = dense down, b_exp = h, b_dense = h_dense (BN-row boxes).
 struct GemmMaps {
   CUtensorMap a_exp, a_dense0, a_dense1, b_exp, b_dense;
+  CUtensorMap a_q;         // int8 expert weights (when the experts are int8)
+  const float* q_scale;    // their row scales
 };
 
 // Launches a kernel with programmatic dependent launch: its CTAs may start while the previous
@@ -141,6 +143,10 @@ cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int 
                         cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
 int gate_up_tiles_per_item(int bn, int T);
+cudaError_t launch_gate_up_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+                              cudaStream_t s);
+cudaError_t launch_down_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+                           cudaStream_t s);
 // SM-pair (cta_group::2) down GEMM for token tiles of 256 (gemm_pair.cu).
 cudaError_t gemm_pair_set_smem_limits();
 int gemm_pair_max_clusters();

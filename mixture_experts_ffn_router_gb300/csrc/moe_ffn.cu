@@ -56,6 +56,20 @@ bool encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols
   return r == CUDA_SUCCESS;
 }
 
+// int8 matrix [rows, cols] row-major, boxes of 128 columns (bytes) x box_rows rows, 128-byte swizzle.
+bool encode_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Split of the router projection over the hidden dimension (a divisor of its 44 chunks of 64):
@@ -167,6 +181,10 @@ struct moe_ffn_ctx {
   const void* cached_dense_gate;
   const void* cached_dense_up;
   const void* cached_dense_down;
+  const void* cached_gate_up_q;
+  const void* cached_down_q;
+  bool cached_valid;
+  CUtensorMap map_gate_up_q, map_down_q;  // int8 experts
   CUtensorMap map_gate_up, map_down, map_dense_gate, map_dense_up, map_dense_down;
   cudaEvent_t ev_start[kKernelsPerForward];
   cudaEvent_t ev_stop[kKernelsPerForward];
@@ -277,11 +295,22 @@ void moe_ffn_destroy(moe_ffn_ctx* ctx) { delete ctx; }
 
 static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
   const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
-  if (!w->router_w || !w->router_norm_w || !w->per_expert_scale || !w->gate_up || !w->down) return MOE_FFN_EINVAL;
+  // int8 experts: all four fields, or none.
+  const bool q8 = w->gate_up_q || w->gate_up_scale || w->down_q || w->down_scale;
+  if (q8) {
+    if (!w->gate_up_q || !w->gate_up_scale || !w->down_q || !w->down_scale) return MOE_FFN_EINVAL;
+    if (!aligned16(w->gate_up_q) || !aligned16(w->down_q) || !aligned16(w->gate_up_scale) ||
+        !aligned16(w->down_scale))
+      return MOE_FFN_EALIGN;
+  }
+  if (!w->router_w || !w->router_norm_w || !w->per_expert_scale || (!q8 && (!w->gate_up || !w->down)))
+    return MOE_FFN_EINVAL;
   if (full && (!w->dense_gate || !w->dense_up || !w->dense_down || !w->pre_ff_ln || !w->pre_ff_ln_2 ||
                !w->post_ff_ln_1 || !w->post_ff_ln_2 || !w->post_ff_ln))
     return MOE_FFN_EINVAL;
-  const void* ps[] = {w->router_w, w->router_norm_w, w->per_expert_scale, w->gate_up, w->down};
+  const void* ps[] = {w->router_w, w->router_norm_w, w->per_expert_scale,
+                      q8 ? static_cast<const void*>(w->gate_up_q) : static_cast<const void*>(w->gate_up),
+                      q8 ? static_cast<const void*>(w->down_q) : static_cast<const void*>(w->down)};
   for (const void* p : ps)
     if (!aligned16(p)) return MOE_FFN_EALIGN;
   if (full) {
@@ -291,11 +320,22 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
       if (!aligned16(p)) return MOE_FFN_EALIGN;
   }
   const bool same = c->cached_gate_up == w->gate_up && c->cached_down == w->down &&
+                    c->cached_gate_up_q == w->gate_up_q && c->cached_down_q == w->down_q &&
                     (!full || (c->cached_dense_gate == w->dense_gate && c->cached_dense_up == w->dense_up &&
                                c->cached_dense_down == w->dense_down));
-  if (same) return MOE_FFN_OK;
-  bool ok = encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
-            encode_bf16(&c->map_down, w->down, static_cast<uint64_t>(E) * H, I, 128);
+  if (same && c->cached_valid) return MOE_FFN_OK;
+  // With int8 experts the bf16 expert maps are never read by a kernel; they are encoded over the
+  // int8 arrays (as bf16 of half as many columns) only so that every map handed to a kernel is valid.
+  bool ok = q8 ? encode_u8(&c->map_gate_up_q, w->gate_up_q, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
+                     encode_u8(&c->map_down_q, w->down_q, static_cast<uint64_t>(E) * H, I, 128) &&
+                     encode_bf16(&c->map_gate_up, w->gate_up_q, static_cast<uint64_t>(E) * 2 * I, H / 2, 64) &&
+                     encode_bf16(&c->map_down, w->down_q, static_cast<uint64_t>(E) * H, I / 2, 128)
+               : encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
+                     encode_bf16(&c->map_down, w->down, static_cast<uint64_t>(E) * H, I, 128);
+  if (!q8) {
+    c->map_gate_up_q = c->map_gate_up;
+    c->map_down_q = c->map_down;
+  }
   if (full)
     ok = ok && encode_bf16(&c->map_dense_gate, w->dense_gate, D, H, 64) &&
          encode_bf16(&c->map_dense_up, w->dense_up, D, H, 64) &&
@@ -306,9 +346,12 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
     c->map_dense_down = c->map_down;
   }
   if (!ok) {
-    c->cached_gate_up = nullptr;
+    c->cached_valid = false;
     return MOE_FFN_ECUDA;
   }
+  c->cached_valid = true;
+  c->cached_gate_up_q = w->gate_up_q;
+  c->cached_down_q = w->down_q;
   c->cached_gate_up = w->gate_up;
   c->cached_down = w->down;
   c->cached_dense_gate = w->dense_gate;
@@ -347,7 +390,9 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   rp.T = T;
   rp.ks = choose_ks(T);
   rp.tpw = choose_tpw(T);
-  rp.bn = choose_bn(T);
+  // int8 experts run the GEMM variants with an int8 weight ring, built for token tiles of up to 64.
+  const bool q8 = w->gate_up_q != nullptr;
+  rp.bn = q8 ? (choose_bn(T) < 64 ? choose_bn(T) : 64) : choose_bn(T);
   rp.full_layer = full ? 1 : 0;
   rp.eps = c->cfg.eps;
   rp.router_scale = c->cfg.router_scale;
@@ -375,13 +420,17 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   dn.a_dense1 = c->map_dense_down;
   dn.b_exp = c->map_h[bk];
   dn.b_dense = c->map_hd[bk];
+  gu.a_q = c->map_gate_up_q;
+  gu.q_scale = w->gate_up_scale;
+  dn.a_q = c->map_down_q;
+  dn.q_scale = w->down_scale;
 
   // Persistent GEMM grids: at most one CTA per SM, and no more than an upper bound of the items.
   const int S = T * K;
   const int bn = rp.bn;
   const int ub_tiles = (S < E ? S : E) + S / bn;
   const int nd = full ? (T + bn - 1) / bn : 0;
-  const int ma = gate_up_tiles_per_item(bn, T);
+  const int ma = q8 ? 1 : gate_up_tiles_per_item(bn, T);
   const long items_gu = static_cast<long>(ub_tiles) * ((I / 64 + ma - 1) / ma) +
                         static_cast<long>(nd) * ((D / 64 + ma - 1) / ma);
   const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
@@ -389,7 +438,7 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
   // For token tiles of 256 (T above 1024) the down GEMM runs on SM pairs: M = 256 per pair of
   // CTAs, half of each token tile in each CTA, so its B maps are the ones with 128-row boxes.
-  const bool pairs = bn == 256 && c->pair_clusters > 0;
+  const bool pairs = bn == 256 && c->pair_clusters > 0 && !q8;
   if (pairs) {
     grid_dn = 2 * c->pair_clusters;
     dn.b_exp = c->map_h[2];
@@ -405,10 +454,14 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
       case 1: e = launch_router_logits(c->map_wsplit, rp, c->buf, s); break;
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
-      case 4: e = launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s); break;
+      case 4:
+        e = q8 ? launch_gate_up_q8(bn, gu, c->buf, T, rp.full_layer, grid_gu, s)
+               : launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s);
+        break;
       case 5:
-        e = pairs ? launch_down_pair(dn, c->buf, T, rp.full_layer, grid_dn, s)
-                  : launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s);
+        e = q8      ? launch_down_q8(bn, dn, c->buf, T, rp.full_layer, grid_dn, s)
+            : pairs ? launch_down_pair(dn, c->buf, T, rp.full_layer, grid_dn, s)
+                    : launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s);
         break;
       case 6: e = launch_combine(cp, c->buf, s); break;
     }
