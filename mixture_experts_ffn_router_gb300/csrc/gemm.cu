@@ -53,7 +53,7 @@ constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 // (1/256 + 1/BN) of the row bytes).
 //
 // Q8: the experts' weights are int8 with one scale per row. A producer warp streams them by TMA into
-// a ring of their own (kRawSlots slots of two K chunks: 128-byte rows, 128-byte swizzle), four
+// a ring of their own (kRawSlots slots of two K chunks: 128-byte rows, 128-byte swizzle), eight
 // converter warps widen each chunk into the bf16 A tile of a stage (one K chunk per stage, in the
 // 128-byte swizzled layout TMA would write), and the epilogue multiplies the accumulator by the
 // row's scale.
@@ -64,7 +64,7 @@ struct Cfg {
   static constexpr int kBChunk = BN * kBK * 2;
   static constexpr int kChunkBytes = kAStage + kBChunk;
   static constexpr int kStageBytes = KC * kChunkBytes;
-  static constexpr int kRawSlots = Q8 ? 6 : 0;                     // int8 weight ring
+  static constexpr int kRawSlots = Q8 ? 4 : 0;                     // int8 weight ring
   static constexpr int kRawSlotBytes = 2 * kBM * kBK;              // two K chunks of 128 int8 rows
   static constexpr int kStagesRaw = (kRingBudget - kRawSlots * kRawSlotBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;

@@ -392,7 +392,9 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   rp.tpw = choose_tpw(T);
   // int8 experts run the GEMM variants with an int8 weight ring, built for token tiles of up to 64.
   const bool q8 = w->gate_up_q != nullptr;
-  rp.bn = q8 ? (choose_bn(T) < 64 ? choose_bn(T) : 64) : choose_bn(T);
+  // int8 experts: stages are one K chunk each, so a narrow token tile buys pipeline depth; small
+  // batches take 32 tokens, larger ones 64.
+  rp.bn = q8 ? (T <= 128 ? 32 : 64) : choose_bn(T);
   rp.full_layer = full ? 1 : 0;
   rp.eps = c->cfg.eps;
   rp.router_scale = c->cfg.router_scale;
