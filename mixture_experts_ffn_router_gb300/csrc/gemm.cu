@@ -52,34 +52,40 @@ constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 // K chunk of the token tile, which cuts the operand bytes per FLOP from (1/128 + 1/BN) to
 // (1/256 + 1/BN) of the row bytes).
 //
-// Q8: the experts' weights are int8 with one scale per row. A producer warp streams them by TMA into
-// a ring of their own (kRawSlots slots of two K chunks: 128-byte rows, 128-byte swizzle), eight
-// converter warps widen each chunk into the bf16 A tile of a stage (one K chunk per stage, in the
-// 128-byte swizzled layout TMA would write), and the epilogue multiplies the accumulator by the
-// row's scale.
+// Q8: the experts' weights are int8 with one scale per row, and the A operand of every MMA comes
+// from tensor memory. A producer warp streams the weight rows by TMA into a ring of their own
+// (kRawSlots slots of 128 rows x 128 bytes, 128-byte swizzle: two int8 K chunks, or one bf16 K
+// chunk of the shared MLP). Eight converter warps, two groups of four taking alternate K chunks,
+// widen each chunk to bf16 (or copy it) into a ring of kASlots A chunks in TMEM; the stages in
+// shared memory hold only B. The epilogue multiplies the accumulator by the row's scale.
 template <int BN, bool GATE_UP, int MA, bool Q8 = false>
 struct Cfg {
   static constexpr int KC = (BN <= 64 && !Q8) ? 2 : 1;
-  static constexpr int kAStage = MA * kAChunk;                     // A bytes of one K chunk
+  static constexpr int kAStage = Q8 ? 0 : MA * kAChunk;            // A bytes of one K chunk in a stage
   static constexpr int kBChunk = BN * kBK * 2;
   static constexpr int kChunkBytes = kAStage + kBChunk;
   static constexpr int kStageBytes = KC * kChunkBytes;
-  static constexpr int kRawSlots = Q8 ? 4 : 0;                     // int8 weight ring
-  static constexpr int kRawSlotBytes = 2 * kBM * kBK;              // two K chunks of 128 int8 rows
+  static constexpr int kRawSlots = Q8 ? (BN <= 32 ? 10 : 8) : 0;   // weight-row ring (Q8)
+  static constexpr int kRawSlotBytes = kBM * 128;                  // 128 rows of 128 bytes
   static constexpr int kStagesRaw = (kRingBudget - kRawSlots * kRawSlotBytes) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kStageCap = Q8 ? 16 : 8;
+  static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
   static constexpr int kEpiWarps = 4 * MA;                         // one per TMEM lane quarter and tile
   static constexpr int kGatherWarps = GATE_UP ? 4 : 0;
   static constexpr int kGatherWarp0 = 2 + kEpiWarps;
   static constexpr int kConvWarps = Q8 ? 8 : 0;                    // int8 -> bf16 converters
   static constexpr int kConvWarp0 = kGatherWarp0 + kGatherWarps;
-  static constexpr int kRawWarp = kConvWarp0 + kConvWarps;         // the int8 producer (Q8)
-  static constexpr int kThreads = (kRawWarp + (Q8 ? 1 : 0)) * 32;
-  static constexpr int kFullArrivals = 1 + kGatherWarps * 32 + kConvWarps;
-  static constexpr int kItemConsumers = 1 + kEpiWarps + kGatherWarps + kConvWarps + (Q8 ? 1 : 0);
+  static constexpr int kRawWarp = kConvWarp0 + kConvWarps;         // the weight-row producer (Q8)
+  static constexpr int kMma2Warp = kRawWarp + 1;                   // the second MMA issuer (Q8)
+  static constexpr int kIssuers = Q8 ? 2 : 1;
+  static constexpr int kThreads = (kRawWarp + (Q8 ? 2 : 0)) * 32;
+  static constexpr int kFullArrivals = 1 + kGatherWarps * 32;
+  static constexpr int kItemConsumers = kIssuers + kEpiWarps + kGatherWarps + kConvWarps + (Q8 ? 1 : 0);
   static constexpr int kAccCols = MA * BN;                         // TMEM columns of one accumulator set
   static constexpr int kNAcc = 2 * kAccCols <= 512 ? 2 : 1;        // double-buffered where it fits
-  static constexpr int kTmemColsRaw = kNAcc * kAccCols;
+  static constexpr int kACol0 = kNAcc * kIssuers * kAccCols;       // Q8: first TMEM column of the A ring
+  static constexpr int kASlots = Q8 ? (512 - kACol0) / 32 : 0;     // Q8: A chunks (128 x 64 bf16 = 32 columns)
+  static constexpr int kTmemColsRaw = Q8 ? 512 : kNAcc * kAccCols;
   static constexpr int kTmemCols = kTmemColsRaw < 32 ? 32 : kTmemColsRaw;
   static constexpr int kTilesExp = GATE_UP ? I / 64 : H / kBM;     // 11 | 22 weight tiles per expert
   static constexpr int kTilesDense = GATE_UP ? D / 64 : H / kBM;   // 33 | 22
@@ -89,7 +95,8 @@ struct Cfg {
   static constexpr int kChunksDense = GATE_UP ? H / kBK : D / kBK; // 44 | 33
   // gate_up: the gate/up hand-over [warps][16][32] fp32; down: a 32x32 output chunk per warp.
   static constexpr int kXchgBytes = kEpiWarps * (GATE_UP ? 16 * 32 * 4 : 32 * 32 * 4);
-  static constexpr int kBarBytes = 512;
+  static constexpr int kBarBytes = Q8 ? 1024 : 512;
+  static constexpr int kBarNeed = 8 * (2 * kStages + 5 + 2 * 8 + 2 * kRawSlots + 2 * kASlots) + 8 + 4 * kStages + 4 * 8;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kRawSlots * kRawSlotBytes + kXchgBytes + kBarBytes;
   static_assert(kChunkBytes % 1024 == 0, "operand tiles must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
@@ -97,7 +104,9 @@ struct Cfg {
   static_assert(kTmemColsRaw <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(kStages >= 2, "stages");
   static_assert(!Q8 || (MA == 1 && KC == 1), "int8 weights: one weight tile per item, one K chunk per stage");
-  static_assert(!Q8 || 128 % (8 * kConvWarps) == 0, "converter rows");
+  static_assert(!Q8 || kConvWarps == 8, "two groups of four converter warps, one per TMEM lane quarter");
+  static_assert(!Q8 || kASlots >= 4, "TMEM A ring");
+  static_assert(kBarNeed <= kBarBytes, "barrier area");
   static_assert(kSmem <= 231424, "shared memory");
 };
 
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint8_t* raw_ring = smem + C::kStages * C::kStageBytes;  // Q8: int8 weight slots
+  uint8_t* raw_ring = smem + C::kStages * C::kStageBytes;  // Q8: weight-row slots
   uint8_t* after_rings = raw_ring + C::kRawSlots * C::kRawSlotBytes;
   float* xchg = reinterpret_cast<float*>(after_rings);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(after_rings + C::kXchgBytes);
@@ -233,12 +242,14 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
   uint64_t* final_bar = acce_bar + 2;
   uint64_t* itemf_bar = final_bar + 1;          // [kItemSlots] item published
   uint64_t* iteme_bar = itemf_bar + kItemSlots; // [kItemSlots] item read by every consumer
-  uint64_t* rawf_bar = iteme_bar + kItemSlots;  // [6] Q8: an int8 slot has landed
-  uint64_t* rawe_bar = rawf_bar + 6;            // [6] Q8: the converters are done with a slot
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rawe_bar + 6);
+  uint64_t* rawf_bar = iteme_bar + kItemSlots;      // [kRawSlots] Q8: a weight slot has landed
+  uint64_t* rawe_bar = rawf_bar + C::kRawSlots;     // [kRawSlots] Q8: the converters are done with it
+  uint64_t* af_bar = rawe_bar + C::kRawSlots;       // [kASlots] Q8: an A chunk is in TMEM
+  uint64_t* ae_bar = af_bar + C::kASlots;           // [kASlots] Q8: the MMAs are done with it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ae_bar + C::kASlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* width_s = reinterpret_cast<int*>(tmem_slot + 2);  // [kStages] MMA width of each stage
-  volatile int* item_s = reinterpret_cast<volatile int*>(width_s + 8);  // [kItemSlots] item ring
+  volatile int* item_s = reinterpret_cast<volatile int*>(width_s + C::kStages);  // [kItemSlots] item ring
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -248,17 +259,21 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < C::kNAcc; ++a) {
-      mbar_init(&accf_bar[a], 1);
+      mbar_init(&accf_bar[a], C::kIssuers);
       mbar_init(&acce_bar[a], C::kEpiWarps);
     }
-    mbar_init(final_bar, 1);
+    mbar_init(final_bar, C::kIssuers);
     for (int k = 0; k < kItemSlots; ++k) {
       mbar_init(&itemf_bar[k], 1);
       mbar_init(&iteme_bar[k], C::kItemConsumers);
     }
     for (int r = 0; r < C::kRawSlots; ++r) {
       mbar_init(&rawf_bar[r], 1);
-      mbar_init(&rawe_bar[r], C::kConvWarps);
+      mbar_init(&rawe_bar[r], C::kConvWarps);  // one arrival per warp (two for a slot read by one group)
+    }
+    for (int a = 0; a < C::kASlots; ++a) {
+      mbar_init(&af_bar[a], C::kConvWarps / 2);
+      mbar_init(&ae_bar[a], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -338,8 +353,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       // gate_up with two tiles: tile 0 holds the gate rows and tile 1 the up rows of 128 features
       // ("paired"); otherwise each tile holds the gate and up rows of 64 features ("stacked").
       const bool paired = GATE_UP && MA == 2 && na == 2;
-      // Q8: the experts' A tiles are written by the converter warps, not by TMA.
-      const bool a_tma = !(Q8 && !it.dense);
+      // Q8: every A chunk reaches tensor memory through the converter warps, not by TMA.
+      const bool a_tma = !Q8;
       for (int c0 = 0; c0 < nch; c0 += C::KC) {
         if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
@@ -403,13 +418,17 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       for (int s2 = 0; s2 < C::kStages; ++s2)
         if (armed & (1u << s2)) mbar_wait_timeout(&full_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs, b.status);
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issuer (one thread)
+  } else if (warp == 1 || (Q8 && warp == C::kMma2Warp)) {
+    // ---------------- MMA issuer (one thread; Q8: two, issuer j taking the item's K chunks with
+    // index parity j, each into its own partial accumulator, which the epilogue adds in that order)
     if (lane == 0) {
+      const int mi = warp == 1 ? 0 : 1;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int aslot = 0;  // Q8: TMEM A ring
+      uint32_t aphase = 0;
       bool ok = true;
       int slot = 0;
       uint32_t slot_par = 0;
@@ -419,39 +438,61 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
         const int nch = (i < n_dense_items) ? C::kChunksDense : C::kChunksExp;
         if (!mbar_wait_bounded(&acce_bar[acc], acc_phase ^ 1u, abort_flag, b.status, kStatusWaitAccEmpty)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+        const uint32_t d_tmem =
+            tmem_base + static_cast<uint32_t>((acc * C::kIssuers + mi) * C::kAccCols);
         uint32_t idesc = 0;
         int na = 1;
+        bool first = true;  // this issuer's first chunk of the item
         for (int c0 = 0; c0 < nch; c0 += C::KC) {
-          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, b.status, kStatusWaitFull)) {
-            ok = false;
-            break;
-          }
-          // The gathered B rows were written by cp.async (generic proxy); the MMA reads them through
-          // the async proxy.
-          if (GATE_UP || Q8) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          tc_fence_after();
-          // The MMA is only as wide as the tile's token rows (rounded up to the MMA's step of 16).
-          if (c0 == 0) {
-            const int ws = width_s[stage];
-            idesc = idesc_bf16_f32(kBM, ws & 0xFFFF);
-            na = ws >> 16;
-          }
-          const int nck = min(C::KC, nch - c0);
-          const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
-          for (int cc = 0; cc < nck; ++cc) {
-            const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + C::kAStage);
-#pragma unroll
-            for (int a = 0; a < MA; ++a) {
-              if (a >= na) break;
-              const uint64_t a_desc = smem_desc_sw128(st + cc * C::kChunkBytes + a * kAChunk);
-#pragma unroll
-              for (int k = 0; k < kBK / 16; ++k)
-                umma_bf16(d_tmem + static_cast<uint32_t>(a * BN), a_desc + 2u * k, b_desc + 2u * k, idesc,
-                          (c0 | cc | k) != 0 ? 1u : 0u);
+          const bool mine = C::kIssuers == 1 || (c0 & 1) == mi;
+          if (mine) {
+            if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, b.status, kStatusWaitFull)) {
+              ok = false;
+              break;
             }
+            if (Q8 && !mbar_wait_bounded(&af_bar[aslot], aphase, abort_flag, b.status, kStatusWaitFull)) {
+              ok = false;
+              break;
+            }
+            // The gathered B rows were written by cp.async (generic proxy); the MMA reads them
+            // through the async proxy.
+            if (GATE_UP || Q8) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_after();
+            // The MMA is only as wide as the tile's token rows (rounded up to the MMA's step of 16).
+            if (first) {
+              const int ws = width_s[stage];
+              idesc = idesc_bf16_f32(kBM, ws & 0xFFFF);
+              na = ws >> 16;
+            }
+            const int nck = min(C::KC, nch - c0);
+            const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
+            for (int cc = 0; cc < nck; ++cc) {
+              const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + C::kAStage);
+              if constexpr (Q8) {
+                const uint32_t a_tm = tmem_base + static_cast<uint32_t>(C::kACol0 + aslot * 32);
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                  umma_bf16_ta(d_tmem, a_tm + 8u * k, b_desc + 2u * k, idesc, (first && k == 0) ? 0u : 1u);
+              } else {
+#pragma unroll
+                for (int a = 0; a < MA; ++a) {
+                  if (a >= na) break;
+                  const uint64_t a_desc = smem_desc_sw128(st + cc * C::kChunkBytes + a * kAChunk);
+#pragma unroll
+                  for (int k = 0; k < kBK / 16; ++k)
+                    umma_bf16(d_tmem + static_cast<uint32_t>(a * BN), a_desc + 2u * k, b_desc + 2u * k, idesc,
+                              (c0 | cc | k) != 0 ? 1u : 0u);
+                }
+              }
+            }
+            first = false;
+            umma_commit(&empty_bar[stage]);
+            if (Q8) umma_commit(&ae_bar[aslot]);
           }
-          umma_commit(&empty_bar[stage]);
+          if (Q8 && ++aslot == C::kASlots) {
+            aslot = 0;
+            aphase ^= 1u;
+          }
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -493,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
         // the two warps of a lane quarter split the token columns.
         const int f = it.m * 128 + 32 * q;
         const uint32_t t_g = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * C::kAccCols);
+                             static_cast<uint32_t>(acc * C::kIssuers * C::kAccCols);
         uint16_t* hs = reinterpret_cast<uint16_t*>(xw + q * 512);  // [32 columns][32 features] bf16
         uint16_t* dst = it.dense ? b.h_dense : b.h;
         const int ld = it.dense ? D : I;
@@ -520,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
         }
       }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * C::kAccCols + ta * BN);
+                             static_cast<uint32_t>(acc * C::kIssuers * C::kAccCols + ta * BN);
       // Q8: this lane's weight row's scale (gate_up: lanes 0..63 gate rows, 64..127 up rows).
       float row_scale = 1.0f;
       if (Q8 && !it.dense && has_tile) {
@@ -534,6 +575,14 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
         float v[32];
         tmem_ld32(t_row + c * 32, v);
         if (Q8) {
+          // The second issuer's partial sum (the item's odd K chunks), added in a fixed order.
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float v2[16];
+            tmem_ld16(t_row + static_cast<uint32_t>(C::kAccCols + c * 32 + 16 * hf), v2);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[16 * hf + j] += v2[j];
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= row_scale;
         }
@@ -682,14 +731,17 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
     }
     cp_async_wait_all();
   } else if (warp < C::kRawWarp) {
-    // ---------------- converters (Q8): chunk h of an int8 slot (K chunks 2j and 2j + 1 of 128 weight
-    // rows) becomes the bf16 A tile of the stage of K chunk 2j + h. Lane l reads 16 bytes (piece
-    // l % 4 of the chunk's 64) of row 8 * step + l / 4 of its warp's 16 rows; with the swizzle the
-    // eight rows of one instruction fall on different banks.
-    const int cw = warp - C::kConvWarp0;
-    const int pl = lane & 3;
-    int stage = 0, r = 0;
-    uint32_t phase = 0, rphase = 0;
+    // ---------------- converters (Q8): weight rows from the raw ring into the TMEM A ring. Group g
+    // (warps 4g..4g+3 of the eight) takes the item's K chunks with index parity g, so two chunks are
+    // in flight; each warp covers the TMEM lane quarter it may access (warp % 4), one weight row per
+    // lane, the chunk's 64 K elements per row.
+    const int grp = (warp - C::kConvWarp0) >> 2;
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const int sw = row & 7;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(C::kACol0);
+    int r = 0, as = 0;
+    uint32_t rphase = 0, aphase = 0;
     bool ok = true;
     int slot = 0;
     uint32_t slot_par = 0;
@@ -698,66 +750,71 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       if (i < 0) break;
       const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
-      for (int c0 = 0; c0 < nch; ++c0) {
-        if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
-          ok = false;
-          break;
-        }
-        if (!it.dense) {
-          const int h = c0 & 1;
-          if (h == 0 && !warp_wait(&rawf_bar[r], rphase, abort_flag, b.status, kStatusWaitFull)) {
+      const bool q8i = !it.dense;  // int8 rows: two K chunks per slot; shared MLP: one bf16 chunk
+      for (int c = 0; c < nch; ++c) {
+        const int h = q8i ? (c & 1) : 0;
+        const bool slot_done = !q8i || h == 1 || c + 1 == nch;
+        if ((c & 1) == grp) {
+          if (!warp_wait(&ae_bar[as], aphase ^ 1u, abort_flag, b.status, kStatusWaitEmpty) ||
+              !warp_wait(&rawf_bar[r], rphase, abort_flag, b.status, kStatusWaitFull)) {
             ok = false;
             break;
           }
-          const uint8_t* raw = raw_ring + r * C::kRawSlotBytes;
-          uint8_t* st = stages + stage * C::kStageBytes;
+          tc_fence_after();
+          const uint8_t* src = raw_ring + r * C::kRawSlotBytes + row * 128;
+          uint32_t o[32];
+          if (q8i) {
+            // 16 int8 per piece, widened exactly: with u = q + 128 (the byte with its top bit
+            // flipped), the fp32 word 0x4B000000 | u is 2^23 + u, so subtracting 2^23 + 128 gives q;
+            // |q| < 256 leaves the low 16 bits zero, so the high halves are the bf16 values.
 #pragma unroll
-          for (int step = 0; step < 128 / (8 * C::kConvWarps); ++step) {
-            const int row = cw * (128 / C::kConvWarps) + step * 8 + (lane >> 2);
-            const int sw = row & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * 128 + (((4 * h + pl) ^ sw) << 4));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint8_t* row_dst = st + row * 128;
+            for (int p = 0; p < 4; ++p) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + (((4 * h + p) ^ sw) << 4));
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint32_t o[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                // Bytes 2(j & 1) and 2(j & 1) + 1 of the word, widened exactly: with u = q + 128
-                // (the byte with its top bit flipped), the fp32 word 0x4B000000 | u is 2^23 + u, so
-                // subtracting 2^23 + 128 gives q; |q| < 256 leaves the low 16 bits zero, so the high
-                // halves are the bf16 values.
-                const uint32_t wx = w4[hh * 2 + (j >> 1)] ^ 0x80808080u;
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t wx = w4[j >> 1] ^ 0x80808080u;
                 const uint32_t k0 = (j & 1) * 2;
                 const float q0 = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | k0)) - 8388736.0f;
                 const float q1 = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | (k0 + 1))) - 8388736.0f;
-                o[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632u);
+                o[8 * p + j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632u);
               }
-              const int piece = 2 * pl + hh;
-              *reinterpret_cast<uint4*>(row_dst + ((piece ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          } else {
+            // bf16 rows: two K elements per 32-bit word already, the lower K in the low half.
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + ((p ^ sw) << 4));
+              o[4 * p] = v.x;
+              o[4 * p + 1] = v.y;
+              o[4 * p + 2] = v.z;
+              o[4 * p + 3] = v.w;
             }
           }
-          // The tile was written through the generic proxy; the MMA reads it through the async proxy.
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tmem_st32(t_lane + static_cast<uint32_t>(as * 32), o);
+          tmem_wait_st();
+          tc_fence_before();
           __syncwarp();
-          if (h == 1 || c0 + 1 == nch) {
-            if (lane == 0) mbar_arrive(&rawe_bar[r]);
-            if (++r == C::kRawSlots) {
-              r = 0;
-              rphase ^= 1u;
-            }
+          if (lane == 0) {
+            mbar_arrive(&af_bar[as]);
+            // A slot holding one chunk is read by this group alone: count both groups' arrivals.
+            if (slot_done) mbar_arrive_n(&rawe_bar[r], (!q8i || h == 0) ? 2u : 1u);
+            else mbar_arrive(&rawe_bar[r]);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full_bar[stage]);
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (++as == C::kASlots) {
+          as = 0;
+          aphase ^= 1u;
+        }
+        if (slot_done && ++r == C::kRawSlots) {
+          r = 0;
+          rphase ^= 1u;
         }
       }
     }
   } else {
-    // ---------------- int8 producer (Q8): the experts' int8 weight rows, two K chunks per slot
+    // ---------------- weight-row producer (Q8): the experts' int8 rows (two K chunks per slot) and
+    // the shared MLP's bf16 rows (one K chunk per slot)
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     int r = 0;
@@ -770,9 +827,10 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       const int i = warp_next_item(itemf_bar, iteme_bar, item_s, slot, slot_par, abort_flag, b.status);
       if (i < 0) break;
       const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
-      if (it.dense) continue;
       const uint64_t pol = it.nt > 2 ? pol_keep : pol_once;
-      for (int c0 = 0; c0 < C::kChunksExp; c0 += 2) {
+      const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
+      const int nslots = it.dense ? nch : (nch + 1) / 2;
+      for (int sidx = 0; sidx < nslots; ++sidx) {
         if (!warp_wait(&rawe_bar[r], rphase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
           break;
@@ -782,12 +840,22 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
           armed_par = (armed_par & ~(1u << r)) | (rphase << r);
           mbar_arrive_expect_tx(&rawf_bar[r], C::kRawSlotBytes);
           uint8_t* dst = raw_ring + r * C::kRawSlotBytes;
-          const int x0 = c0 * kBK;  // int8: one byte per element
-          if (GATE_UP) {
-            tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + it.m * 64, pol);
-            tma_load_2d(dst + 64 * 128, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + I + it.m * 64, pol);
+          if (it.dense) {
+            const int k0 = sidx * kBK;
+            if (GATE_UP) {
+              tma_load_2d(dst, &map_a_d0, &rawf_bar[r], k0, it.m * 64, pol);
+              tma_load_2d(dst + 64 * 128, &map_a_d1, &rawf_bar[r], k0, it.m * 64, pol);
+            } else {
+              tma_load_2d(dst, &map_a_d0, &rawf_bar[r], k0, it.m * kBM, pol);
+            }
           } else {
-            tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * H + it.m * kBM, pol);
+            const int x0 = sidx * 2 * kBK;  // int8: one byte per element
+            if (GATE_UP) {
+              tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + it.m * 64, pol);
+              tma_load_2d(dst + 64 * 128, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + I + it.m * 64, pol);
+            } else {
+              tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * H + it.m * kBM, pol);
+            }
           }
         }
         __syncwarp();
