@@ -17,6 +17,10 @@ Pins (what the oracle is checked against, in ``tests/test_oracle_pins.py``):
   * The permutation against a brute-force sort of the slots by (expert, token).
   * int8 experts: the quantiser's error bound, symmetry, exact rows and zero rows; the layer with
     int8 experts against brute.py on the dequantised weights.
+  * MXFP4 experts (``tests/test_oracle_fp4.py``): the shared-exponent rule (every block's maximum
+    lands in [4, 8) scale units), exact grid values, the per-interval error bound and saturation,
+    ties to the even code, symmetry, zero blocks; the layer with MXFP4 experts against brute.py on
+    the dequantised weights.
 """
 import ctypes
 
@@ -66,6 +70,10 @@ class Weights(ctypes.Structure):
         ("gate_up_scale", _f32p),
         ("down_q", ctypes.POINTER(ctypes.c_int8)),
         ("down_scale", _f32p),
+        ("gate_up_f4", ctypes.POINTER(ctypes.c_uint8)),
+        ("gate_up_f4s", ctypes.POINTER(ctypes.c_uint8)),
+        ("down_f4", ctypes.POINTER(ctypes.c_uint8)),
+        ("down_f4s", ctypes.POINTER(ctypes.c_uint8)),
     ]
 
 
@@ -108,6 +116,9 @@ def lib():
         L.moe_oracle_quantize_int8.restype = ctypes.c_int
         L.moe_oracle_quantize_int8.argtypes = [_u16p, ctypes.c_longlong, ctypes.c_int,
                                                ctypes.POINTER(ctypes.c_int8), _f32p]
+        L.moe_oracle_quantize_mxfp4.restype = ctypes.c_int
+        L.moe_oracle_quantize_mxfp4.argtypes = [_u16p, ctypes.c_longlong, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
         L.moe_oracle_set_threads.restype = None
         L.moe_oracle_set_threads.argtypes = [ctypes.c_int]
         L.moe_oracle_max_threads.restype = ctypes.c_int
@@ -197,6 +208,16 @@ def forward(dims: dict, x_bf16: np.ndarray, weights: dict, want=("out",), masked
             keep[f.replace("_q", "_scale")] = sc
             setattr(wst, f.replace("_q", "_scale"), _ptr(sc, ctypes.c_float))
             keep.setdefault(f.replace("_q", ""), a)  # the bf16 form is not needed
+    for f in ("gate_up_f4", "down_f4"):
+        a = weights.get(f)
+        if a is not None:
+            a = _as(a, np.uint8)
+            keep[f] = a
+            setattr(wst, f, _ptr(a, ctypes.c_uint8))
+            sc = _as(weights[f + "s"], np.uint8)
+            keep[f + "s"] = sc
+            setattr(wst, f + "s", _ptr(sc, ctypes.c_uint8))
+            keep.setdefault(f.replace("_f4", ""), a)  # the bf16 form is not needed
     wst.layer_scalar = float(weights.get("layer_scalar", 1.0))
     if route_only:
         missing = [f for f in ("router_w", "router_norm_w", "per_expert_scale") if f not in keep]
@@ -250,6 +271,34 @@ def quantize_int8(w_bf16: np.ndarray):
     return q, scale
 
 
+def quantize_mxfp4(w_bf16: np.ndarray):
+    """MXFP4 quantisation of a bf16 matrix [.., cols], cols a multiple of 32 (see
+    moe_oracle_quantize_mxfp4). Returns (codes uint8 [rows, cols / 2], scales uint8 [rows, cols / 32])."""
+    w = _as(np.asarray(w_bf16), np.uint16)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, max(cols // 32, 1)), np.uint8)
+    rc = lib().moe_oracle_quantize_mxfp4(_ptr(w, ctypes.c_uint16), rows, cols, _ptr(codes, ctypes.c_uint8),
+                                         _ptr(scales, ctypes.c_uint8))
+    if rc != 0:
+        raise ValueError("moe_oracle_quantize_mxfp4: bad arguments")
+    return codes, scales
+
+
+E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def dequantize_mxfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The float64 weights an MXFP4 matrix stands for (codes [rows, cols / 2], scales [rows, cols / 32])."""
+    codes = np.asarray(codes, np.uint8)
+    nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+    mag = E2M1[nib & 7]
+    val = np.where(nib & 8, -mag, mag)
+    e = np.repeat(np.asarray(scales, np.int64) - 127, 32, axis=1)
+    return np.ldexp(val, e)
+
+
 def permute(topk_idx: np.ndarray, topk_w, n_experts: int) -> dict:
     """Stable counting sort of the slots by expert (see moe_oracle_permute)."""
     idx = _as(np.asarray(topk_idx), np.int32)
@@ -276,5 +325,6 @@ def gemma_dims(full_layer: bool) -> dict:
             "full_layer": int(bool(full_layer)), "eps": 1e-6, "router_scale": 2816 ** -0.5}
 
 
-__all__ = ["lib", "gelu_tanh", "rmsnorm", "forward", "permute", "quantize_int8", "set_threads", "max_threads",
+__all__ = ["lib", "gelu_tanh", "rmsnorm", "forward", "permute", "quantize_int8", "quantize_mxfp4",
+           "dequantize_mxfp4", "set_threads", "max_threads",
            "gemma_dims", "Dims", "Weights", "Outputs"]

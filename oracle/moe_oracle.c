@@ -110,10 +110,21 @@ static void route_one(const moe_oracle_dims* d, const float* xin, const moe_orac
   }
 }
 
-/* Element (row, col) of an expert weight matrix with `cols` columns: the bf16 value, or, when the
- * int8 form is given, q * scale of the row (exact in fp64: q has 8 bits, scale 24). */
-static double expert_weight(const uint16_t* bf, const int8_t* q, const float* scale, size_t row, size_t col,
-                            size_t cols) {
+/* The E2M1 magnitudes, by the 3-bit magnitude code. */
+static const double kE2M1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Element (row, col) of an expert weight matrix with `cols` columns: the bf16 value; or, when the
+ * int8 form is given, q * scale of the row (exact in fp64: q has 8 bits, scale 24); or, when the
+ * MXFP4 form is given, the E2M1 value of its code times its block's power-of-two scale (exact). */
+static double expert_weight(const uint16_t* bf, const int8_t* q, const float* scale, const uint8_t* f4,
+                            const uint8_t* f4s, size_t row, size_t col, size_t cols) {
+  if (f4) {
+    const uint8_t byte = f4[row * (cols / 2) + col / 2];
+    const int code = (col & 1) ? (byte >> 4) : (byte & 15);
+    const double mag = kE2M1[code & 7];
+    const int e = (int)f4s[row * (cols / 32) + col / 32] - 127;
+    return ldexp((code & 8) ? -mag : mag, e);
+  }
   if (q) return (double)q[row * cols + col] * (double)scale[row];
   return (double)bf16_to_f32(bf[row * cols + col]);
 }
@@ -129,15 +140,15 @@ static void expert_mlp(const moe_oracle_dims* d, const moe_oracle_weights* w, in
   for (int i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     for (int h = 0; h < H; ++h) {
-      g += expert_weight(w->gate_up, w->gate_up_q, w->gate_up_scale, g0 + i, h, H) * v[h];
-      u += expert_weight(w->gate_up, w->gate_up_q, w->gate_up_scale, g0 + I + i, h, H) * v[h];
+      g += expert_weight(w->gate_up, w->gate_up_q, w->gate_up_scale, w->gate_up_f4, w->gate_up_f4s, g0 + i, h, H) * v[h];
+      u += expert_weight(w->gate_up, w->gate_up_q, w->gate_up_scale, w->gate_up_f4, w->gate_up_f4s, g0 + I + i, h, H) * v[h];
     }
     hvec[i] = moe_oracle_gelu_tanh(g) * u;
   }
   const size_t d0 = (size_t)e * H;  /* first down row of expert e */
   for (int h = 0; h < H; ++h) {
     double acc = 0.0;
-    for (int i = 0; i < I; ++i) acc += expert_weight(w->down, w->down_q, w->down_scale, d0 + h, i, I) * hvec[i];
+    for (int i = 0; i < I; ++i) acc += expert_weight(w->down, w->down_q, w->down_scale, w->down_f4, w->down_f4s, d0 + h, i, I) * hvec[i];
     y[h] = acc;
   }
 }
@@ -174,8 +185,10 @@ static int dims_ok(const moe_oracle_dims* d) {
 int moe_oracle_forward(const moe_oracle_dims* d, int T, const uint16_t* x,
                        const moe_oracle_weights* w, const moe_oracle_outputs* o, int masked_dense) {
   if (!dims_ok(d) || T < 0 || !w || !o || (T > 0 && !x)) return -1;
-  if ((!w->gate_up && !(w->gate_up_q && w->gate_up_scale)) || (!w->down && !(w->down_q && w->down_scale)))
+  if ((!w->gate_up && !(w->gate_up_q && w->gate_up_scale) && !(w->gate_up_f4 && w->gate_up_f4s)) ||
+      (!w->down && !(w->down_q && w->down_scale) && !(w->down_f4 && w->down_f4s)))
     return -1;
+  if ((w->gate_up_f4 && d->hidden % 32 != 0) || (w->down_f4 && d->moe_inter % 32 != 0)) return -1;
   const int H = d->hidden, E = d->n_experts, K = d->top_k, I = d->moe_inter;
   const int D = d->full_layer ? d->dense_inter : 1;
   int bad = 0;
@@ -344,6 +357,58 @@ int moe_oracle_quantize_int8(const uint16_t* w, long long rows, int cols, int8_t
         if (v < -127.0f) v = -127.0f;
       }
       q[(size_t)r * cols + c] = (int8_t)v;
+    }
+  }
+  return 0;
+}
+
+/* E2M1 code of v (the element already divided by its block scale): the nearest of the E2M1
+ * magnitudes, ties to the even code (the one whose mantissa bit, bit 0 of the code, is 0),
+ * magnitudes above 6 saturated to 6; the sign in bit 3, zero as +0. */
+static int e2m1_code(double v) {
+  const double a = fabs(v);
+  int best = 0;
+  for (int k = 1; k < 8; ++k) {
+    const double dk = fabs(a - kE2M1[k]), db = fabs(a - kE2M1[best]);
+    if (dk < db || (dk == db && (k & 1) == 0)) best = k;
+  }
+  if (a > 6.0) best = 7;
+  return (best != 0 && v < 0) ? (best | 8) : best;
+}
+
+int moe_oracle_quantize_mxfp4(const uint16_t* w, long long rows, int cols, uint8_t* codes, uint8_t* scales) {
+  if (!w || !codes || !scales || rows < 0 || cols < 32 || cols % 32 != 0) return -1;
+  const int nb = cols / 32;
+  for (long long r = 0; r < rows; ++r) {
+    const uint16_t* wr = w + (size_t)r * cols;
+    for (int b = 0; b < nb; ++b) {
+      /* 1. the block's largest magnitude */
+      double amax = 0.0;
+      for (int j = 0; j < 32; ++j) {
+        const double a = fabs((double)bf16_to_f32(wr[b * 32 + j]));
+        if (a > amax) amax = a;
+      }
+      /* 2. the shared exponent floor(log2 amax) - emax(E2M1) = ... - 2, in the E8M0 range */
+      int se = 0;
+      uint8_t sbyte = 0;
+      if (amax > 0.0) {
+        int ex;
+        frexp(amax, &ex); /* amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
+        se = (ex - 1) - 2;
+        if (se < -127) se = -127;
+        if (se > 127) se = 127;
+        sbyte = (uint8_t)(se + 127);
+      }
+      scales[(size_t)r * nb + b] = sbyte;
+      /* 3. every element divided by the scale 2^se and rounded to E2M1 */
+      for (int j = 0; j < 32; j += 2) {
+        int c0 = 0, c1 = 0;
+        if (amax > 0.0) {
+          c0 = e2m1_code(ldexp((double)bf16_to_f32(wr[b * 32 + j]), -se));
+          c1 = e2m1_code(ldexp((double)bf16_to_f32(wr[b * 32 + j + 1]), -se));
+        }
+        codes[(size_t)r * (cols / 2) + (b * 32 + j) / 2] = (uint8_t)(c0 | (c1 << 4));
+      }
     }
   }
   return 0;

@@ -68,6 +68,16 @@ typedef struct moe_oracle_weights {
   const float* gate_up_scale;     /* [E * 2I] */
   const int8_t* down_q;           /* [E * H, I] */
   const float* down_scale;        /* [E * H] */
+  /* Optional MXFP4 form of the expert weights (the microscaling fp4 format [MoE] "The fp4 rabbit
+   * hole" names: blocks of 32 consecutive elements of a row share one scale). When gate_up_f4 is
+   * set, expert weight (row, col) of gate_up is e2m1(code) * 2^(gate_up_f4s[row, col / 32] - 127),
+   * code = the low nibble of byte gate_up_f4[row, col / 2] for even col, the high nibble for odd
+   * col (bit 3 the sign, bits 2..0 the magnitude index into {0, 0.5, 1, 1.5, 2, 3, 4, 6}); gate_up
+   * and gate_up_q may then be NULL. Likewise for down. */
+  const uint8_t* gate_up_f4;      /* [E * 2I, H / 2] */
+  const uint8_t* gate_up_f4s;     /* [E * 2I, H / 32] */
+  const uint8_t* down_f4;         /* [E * H, I / 2] */
+  const uint8_t* down_f4s;        /* [E * H, I / 32] */
 } moe_oracle_weights;
 
 /* Every field may be NULL (not written). Slot (t, k): token t's k-th selected expert, k in
@@ -110,6 +120,17 @@ int moe_oracle_route(const moe_oracle_dims* d, int T, const uint16_t* x, const m
  * ties to even, clamped to [-127, 127]; an all-zero row gets scale 0 and q 0. Returns 0, or -1 on
  * bad arguments. */
 int moe_oracle_quantize_int8(const uint16_t* w, long long rows, int cols, int8_t* q, float* scale);
+
+/* MXFP4 quantisation of a bf16 matrix [rows, cols] (cols a multiple of 32), after the OCP
+ * Microscaling Formats (MX) v1.0 conversion: for each block of 32 consecutive elements of a row,
+ * amax = max |w|; if amax > 0 the shared exponent is floor(log2 amax) - 2 (2 = the largest exponent
+ * of E2M1), clamped to [-127, 127], and the block scale X = 2^that; each element w / X is rounded to
+ * the nearest E2M1 value (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; ties to the even code), and
+ * magnitudes above 6 saturate to 6. A value that rounds to zero is stored as code 0 (+0). An
+ * all-zero block gets scale byte 0 and codes 0. scales[r, b] = shared exponent + 127 (E8M0);
+ * codes[r, c / 2] holds element c in its low nibble (even c) or high nibble (odd c). Returns 0,
+ * or -1 on bad arguments. */
+int moe_oracle_quantize_mxfp4(const uint16_t* w, long long rows, int cols, uint8_t* codes, uint8_t* scales);
 
 /* Stable counting sort of the T*K slots by expert: counts[E], offsets[E+1] (exclusive prefix sum,
  * offsets[E] = T*K), perm[T*K] (token of each sorted slot; within one expert tokens ascend),
