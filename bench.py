@@ -46,6 +46,9 @@ WORKLOADS = {
     "decode64_int8": dict(full=True, T=64, skew=False, int8=True,
                           desc="Gemma-4 26B-A4B full dual-path FFN layer, decode batch T=64, uniform routing, "
                                "int8 per-channel experts"),
+    "decode64_fp4": dict(full=True, T=64, skew=False, fp4=True,
+                         desc="Gemma-4 26B-A4B full dual-path FFN layer, decode batch T=64, uniform routing, "
+                              "MXFP4 experts"),
     "moe8": dict(full=False, T=8, skew=False, desc="Gemma-4 26B-A4B MoE block only (router + experts), T=8"),
     "layer": dict(full=True, T=None, skew=False, desc="Gemma-4 26B-A4B full dual-path FFN layer, uniform routing"),
     "stack30": dict(full=True, T=256, skew=False, layers=30,
@@ -241,6 +244,10 @@ def run_reference(args, wl):
         for name, cols in (("gate_up", H), ("down", I)):
             q, sc = oracle.quantize_int8(w.pop(name).reshape(-1, cols))
             w[name + "_q"], w[name + "_scale"] = q, sc
+    if wl.get("fp4"):
+        for name, cols in (("gate_up", H), ("down", I)):
+            c4, s4 = oracle.quantize_mxfp4(w.pop(name).reshape(-1, cols))
+            w[name + "_f4"], w[name + "_f4s"] = c4, s4
     x = synth.bf16_bits(synth.make_x(T, seed=args.seed, device="cpu"))[:n]
     dims = oracle.gemma_dims(wl["full"])
     for _ in range(max(args.warmup, 0)):
@@ -283,9 +290,10 @@ def run_ours(args, wl):
     # One context per layer, all sharing the first one's workspace (their forwards never overlap).
     weights = [synth.make_weights(seed=args.seed, layer=l, device=dev, full_layer=wl["full"], skew=wl["skew"])
                for l in range(L)]
-    if wl.get("int8"):
-        # int8 experts, made on the device; the bf16 experts are then dropped.
-        weights = [B.quantize_experts_int8(w) for w in weights]
+    if wl.get("int8") or wl.get("fp4"):
+        # int8 or MXFP4 experts, made on the device; the bf16 experts are then dropped.
+        q = B.quantize_experts_int8 if wl.get("int8") else B.quantize_experts_mxfp4
+        weights = [q(w) for w in weights]
         torch.cuda.synchronize()
         for w in weights:
             del w["gate_up"], w["down"]
@@ -393,9 +401,14 @@ def run_ours(args, wl):
     hbm, tc_burst, tc_sus, peak_src = measured_peaks()
     S = T * K
     full = wl["full"]
-    # int8 experts: one byte per weight plus a 4-byte scale per row.
-    gu_pe = (2 * I * H + 2 * I * 4) if wl.get("int8") else GATE_UP_BYTES_PER_EXPERT
-    dn_pe = (H * I + H * 4) if wl.get("int8") else DOWN_BYTES_PER_EXPERT
+    # int8 experts: one byte per weight plus a 4-byte scale per row; MXFP4: half a byte per weight
+    # plus a 1-byte scale per 32 weights.
+    if wl.get("int8"):
+        gu_pe, dn_pe = 2 * I * H + 2 * I * 4, H * I + H * 4
+    elif wl.get("fp4"):
+        gu_pe, dn_pe = 2 * I * H // 2 + 2 * I * H // 32, H * I // 2 + H * I // 32
+    else:
+        gu_pe, dn_pe = GATE_UP_BYTES_PER_EXPERT, DOWN_BYTES_PER_EXPERT
     gu_bytes = experts_hit * gu_pe + (DENSE_GATE_UP_BYTES if full else 0) \
         + T * H * 2 * (2 if full else 1) + S * I * 2 + (T * D * 2 if full else 0)
     gu_flops = 2 * S * 2 * I * H + (2 * T * 2 * D * H if full else 0)
@@ -463,7 +476,8 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl["desc"], "T": T, "tokens_per_gpu": T, "hidden": H, "experts": E, "top_k": K,
                        "moe_inter": I, "dense_inter": D if wl["full"] else 0,
-                       "expert_weights": "int8, per-row fp32 scale" if wl.get("int8") else "bf16",
+                       "expert_weights": ("int8, per-row fp32 scale" if wl.get("int8") else
+                                          "MXFP4 (E2M1, E8M0 scale per 32 weights)" if wl.get("fp4") else "bf16"),
                        "layers": L,
                        "l2": "inputs larger than L2 (%.2f GB of weights read per step)" % (layer_bytes * L / 1e9),
                        "parallelism": "replicas (dp%d, no collective)" % world},

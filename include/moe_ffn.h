@@ -101,6 +101,17 @@ typedef struct moe_ffn_weights {
   const float* gate_up_scale;     /* [128 * 1408] fp32, one per row */
   const int8_t* down_q;           /* [128 * 2816, 704] int8 */
   const float* down_scale;        /* [128 * 2816] fp32, one per row */
+  /* Optional MXFP4 experts (the microscaling fp4 format of the same post, section "The fp4 rabbit
+   * hole": blocks of 32 consecutive elements of a row share one power-of-two scale). When
+   * gate_up_f4 is not NULL, all four fields must be set and the int8 fields must be NULL; expert
+   * weight (row, col) is then e2m1(code) * 2^(scale byte - 127), where the code is the low nibble
+   * of byte [row, col / 2] for even col and the high nibble for odd col (bit 3 the sign, bits 2..0
+   * index the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) and the scale byte is [row, col / 32] (E8M0).
+   * gate_up / down are not read (the shared MLP stays bf16). moe_ffn_quantize_mxfp4 makes them. */
+  const uint8_t* gate_up_f4;      /* [128 * 1408, 1408] packed E2M1 codes */
+  const uint8_t* gate_up_f4s;     /* [128 * 1408, 88] E8M0 block scales */
+  const uint8_t* down_f4;         /* [128 * 2816, 352] packed E2M1 codes */
+  const uint8_t* down_f4s;        /* [128 * 2816, 22] E8M0 block scales */
 } moe_ffn_weights;
 
 /* Device views into the workspace, filled by moe_ffn_workspace_view. Contents are those of the
@@ -189,7 +200,6 @@ int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
 int moe_ffn_router_logits_noalloc(const void* x, int T, const float* router_w, const float* router_norm_w,
                                   float router_scale, float eps, float* logits, void* stream);
 
-/* A static string naming a status code. */
 /* Per-channel symmetric int8 quantisation of a bf16 matrix [rows, cols] on the device, one channel
  * per row: scale[r] = max_c |w[r, c]| / 127 in fp32, q[r, c] = w[r, c] / scale[r] in fp32 rounded
  * to nearest (ties to even) and clamped to [-127, 127]; an all-zero row gets scale 0 and q 0. All
@@ -198,6 +208,19 @@ int moe_ffn_router_logits_noalloc(const void* x, int T, const float* router_w, c
  * fails. */
 int moe_ffn_quantize_int8(const void* w, long long rows, int cols, int8_t* q, float* scale, void* stream);
 
+/* MXFP4 quantisation of a bf16 matrix [rows, cols] on the device, after the OCP Microscaling
+ * Formats (MX) v1.0 conversion: for each block of 32 consecutive elements of a row, amax = max |w|;
+ * if amax > 0 the shared exponent is floor(log2 amax) - 2, clamped to [-127, 127], and every
+ * element w / 2^exponent is rounded to the nearest E2M1 magnitude (0, 0.5, 1, 1.5, 2, 3, 4, 6; ties
+ * to the even code; above 6 saturates to 6) with its sign; a value that rounds to zero is +0 (code
+ * 0). An all-zero block gets scale byte 0 and codes 0. codes[r, c / 2] holds element c in its low
+ * (even c) or high (odd c) nibble; scales[r, c / 32] = exponent + 127. All pointers are device
+ * pointers; w and codes 16-byte aligned, cols a multiple of 32. Asynchronous on `stream`. Returns
+ * MOE_FFN_EINVAL / MOE_FFN_EALIGN on bad arguments, MOE_FFN_ECUDA if the launch fails. */
+int moe_ffn_quantize_mxfp4(const void* w, long long rows, int cols, uint8_t* codes, uint8_t* scales,
+                           void* stream);
+
+/* A static string naming a status code. */
 const char* moe_ffn_status_string(int status);
 
 /* Releases the host state of a context (it holds no device memory). Never frees the workspace or

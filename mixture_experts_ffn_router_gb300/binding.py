@@ -37,10 +37,12 @@ WEIGHT_FIELDS = ("router_w", "router_norm_w", "per_expert_scale", "gate_up", "do
 
 
 INT8_FIELDS = ("gate_up_q", "gate_up_scale", "down_q", "down_scale")
+F4_FIELDS = ("gate_up_f4", "gate_up_f4s", "down_f4", "down_f4s")
 
 
 class moe_ffn_weights(ctypes.Structure):
-    _fields_ = [(f, _vp) for f in WEIGHT_FIELDS] + [("layer_scalar", ctypes.c_float)] + [(f, _vp) for f in INT8_FIELDS]
+    _fields_ = ([(f, _vp) for f in WEIGHT_FIELDS] + [("layer_scalar", ctypes.c_float)] + [(f, _vp) for f in INT8_FIELDS]
+                + [(f, _vp) for f in F4_FIELDS])
 
 
 VIEW_FIELDS = ("logits", "topk_idx", "topk_w", "gap", "counts", "offsets", "perm", "w_sorted", "slot_pos", "n1",
@@ -84,6 +86,8 @@ def lib():
         L.moe_ffn_status_string.argtypes = [ctypes.c_int]
         L.moe_ffn_quantize_int8.restype = ctypes.c_int
         L.moe_ffn_quantize_int8.argtypes = [_vp, ctypes.c_longlong, ctypes.c_int, _vp, _vp, _vp]
+        L.moe_ffn_quantize_mxfp4.restype = ctypes.c_int
+        L.moe_ffn_quantize_mxfp4.argtypes = [_vp, ctypes.c_longlong, ctypes.c_int, _vp, _vp, _vp]
         L.moe_ffn_destroy.restype = None
         L.moe_ffn_destroy.argtypes = [_vp]
         _LIB = L
@@ -177,6 +181,27 @@ def quantize_experts_int8(w: dict) -> dict:
     return out
 
 
+def moe_ffn_quantize_mxfp4(w: int, rows: int, cols: int, codes: int, scales: int, stream: int) -> int:
+    return lib().moe_ffn_quantize_mxfp4(_vp(w), int(rows), int(cols), _vp(codes), _vp(scales), _vp(stream))
+
+
+def quantize_experts_mxfp4(w: dict) -> dict:
+    """Adds the MXFP4 form of the experts (gate_up_f4/f4s, down_f4/f4s) to a dict of CUDA weight
+    tensors, made on the device by moe_ffn_quantize_mxfp4."""
+    import torch
+    out = dict(w)
+    s = torch.cuda.current_stream().cuda_stream
+    for name, rows, cols in (("gate_up", N_EXPERTS * 2 * MOE_INTER, HIDDEN), ("down", N_EXPERTS * HIDDEN, MOE_INTER)):
+        src = w[name]
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=src.device)
+        sc = torch.empty((rows, cols // 32), dtype=torch.uint8, device=src.device)
+        _check("moe_ffn_quantize_mxfp4",
+               moe_ffn_quantize_mxfp4(src.data_ptr(), rows, cols, codes.data_ptr(), sc.data_ptr(), s))
+        out[name + "_f4"] = codes
+        out[name + "_f4s"] = sc
+    return out
+
+
 def moe_ffn_destroy(ctx: int) -> None:
     lib().moe_ffn_destroy(_vp(ctx))
 
@@ -186,7 +211,7 @@ def moe_ffn_destroy(ctx: int) -> None:
 def weights_struct(w: dict) -> moe_ffn_weights:
     """A moe_ffn_weights whose fields point at the CUDA tensors of ``w`` (absent fields are NULL)."""
     s = moe_ffn_weights()
-    for f in WEIGHT_FIELDS + INT8_FIELDS:
+    for f in WEIGHT_FIELDS + INT8_FIELDS + F4_FIELDS:
         t = w.get(f)
         if t is not None:
             if not t.is_cuda or not t.is_contiguous():

@@ -58,8 +58,14 @@ constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 // chunk of the shared MLP). Eight converter warps, two groups of four taking alternate K chunks,
 // widen each chunk to bf16 (or copy it) into a ring of kASlots A chunks in TMEM; the stages in
 // shared memory hold only B. The epilogue multiplies the accumulator by the row's scale.
-template <int BN, bool GATE_UP, int MA, bool Q8 = false>
+// QW: the experts' weight format, 0 bf16, 1 int8 (kWInt8), 2 MXFP4 (kWFp4); Q8 = converted weights.
+constexpr int kWBf16 = 0, kWInt8 = 1, kWFp4 = 2;
+
+template <int BN, bool GATE_UP, int MA, int QW = kWBf16>
 struct Cfg {
+  static constexpr bool Q8 = QW != kWBf16;
+  static constexpr bool F4 = QW == kWFp4;
+  static constexpr int kExpChunksPerSlot = F4 ? 4 : 2;           // K chunks in a weight-row slot (Q8)
   static constexpr int KC = (BN <= 64 && !Q8) ? 2 : 1;
   static constexpr int kAStage = Q8 ? 0 : MA * kAChunk;            // A bytes of one K chunk in a stage
   static constexpr int kBChunk = BN * kBK * 2;
@@ -222,13 +228,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
-template <int BN, bool GATE_UP, int MA, bool Q8>
-__global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
+template <int BN, bool GATE_UP, int MA, int QW>
+__global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a_exp, const __grid_constant__ CUtensorMap map_a_d0,
                         const __grid_constant__ CUtensorMap map_a_d1, const __grid_constant__ CUtensorMap map_b_exp,
                         const __grid_constant__ CUtensorMap map_b_dense, Buffers b, int T, int full_layer,
-                        const __grid_constant__ CUtensorMap map_q, const float* q_scale) {
-  using C = Cfg<BN, GATE_UP, MA, Q8>;
+                        const __grid_constant__ CUtensorMap map_q, const void* q_scale) {
+  using C = Cfg<BN, GATE_UP, MA, QW>;
+  constexpr bool Q8 = C::Q8;
+  constexpr bool F4 = C::F4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -564,10 +572,10 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
                              static_cast<uint32_t>(acc * C::kIssuers * C::kAccCols + ta * BN);
       // Q8: this lane's weight row's scale (gate_up: lanes 0..63 gate rows, 64..127 up rows).
       float row_scale = 1.0f;
-      if (Q8 && !it.dense && has_tile) {
+      if (Q8 && !F4 && !it.dense && has_tile) {
         const size_t row = GATE_UP ? static_cast<size_t>(it.e) * (2 * I) + (q < 2 ? 0 : I) + tile * 64 + 32 * (q & 1) + lane
                                    : static_cast<size_t>(it.e) * H + tile * kBM + 32 * q + lane;
-        row_scale = __ldg(q_scale + row);
+        row_scale = __ldg(static_cast<const float*>(q_scale) + row);
       }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -734,7 +742,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
     // ---------------- converters (Q8): weight rows from the raw ring into the TMEM A ring. Group g
     // (warps 4g..4g+3 of the eight) takes the item's K chunks with index parity g, so two chunks are
     // in flight; each warp covers the TMEM lane quarter it may access (warp % 4), one weight row per
-    // lane, the chunk's 64 K elements per row.
+    // lane, the chunk's 64 K elements per row. A raw slot holds cps chunks of every row (int8 2,
+    // MXFP4 4, the shared MLP's bf16 1); each warp releases it after the last of its chunks there.
     const int grp = (warp - C::kConvWarp0) >> 2;
     const int q = warp & 3;
     const int row = 32 * q + lane;
@@ -750,11 +759,25 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       if (i < 0) break;
       const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
-      const bool q8i = !it.dense;  // int8 rows: two K chunks per slot; shared MLP: one bf16 chunk
+      const bool cvt = !it.dense;  // the experts' converted rows; the shared MLP's rows are bf16
+      const int cps = cvt ? C::kExpChunksPerSlot : 1;
+      // MXFP4: this row's E8M0 scales, two per K chunk (blocks of 32).
+      const uint8_t* srow = nullptr;
+      if (F4 && cvt) {
+        const size_t grow = GATE_UP ? static_cast<size_t>(it.e) * (2 * I) + (row < 64 ? 0 : I) + it.m * 64 + (row & 63)
+                                    : static_cast<size_t>(it.e) * H + it.m * kBM + row;
+        srow = static_cast<const uint8_t*>(q_scale) + grow * (GATE_UP ? H / 32 : I / 32);
+      }
+      // The scales of this group's next chunk are loaded one chunk ahead.
+      uint32_t sc_next = 0;
+      if (F4 && cvt && grp < nch) sc_next = __ldg(reinterpret_cast<const unsigned short*>(srow + 2 * grp));
       for (int c = 0; c < nch; ++c) {
-        const int h = q8i ? (c & 1) : 0;
-        const bool slot_done = !q8i || h == 1 || c + 1 == nch;
+        const int slot_lo = c - c % cps;
+        const int slot_hi = min(slot_lo + cps, nch);
+        const int j = c - slot_lo;  // chunk within the slot
         if ((c & 1) == grp) {
+          const uint32_t sc2 = sc_next;
+          if (F4 && cvt && c + 2 < nch) sc_next = __ldg(reinterpret_cast<const unsigned short*>(srow + 2 * (c + 2)));
           if (!warp_wait(&ae_bar[as], aphase ^ 1u, abort_flag, b.status, kStatusWaitEmpty) ||
               !warp_wait(&rawf_bar[r], rphase, abort_flag, b.status, kStatusWaitFull)) {
             ok = false;
@@ -763,21 +786,59 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
           tc_fence_after();
           const uint8_t* src = raw_ring + r * C::kRawSlotBytes + row * 128;
           uint32_t o[32];
-          if (q8i) {
+          if (cvt && !F4) {
             // 16 int8 per piece, widened exactly: with u = q + 128 (the byte with its top bit
             // flipped), the fp32 word 0x4B000000 | u is 2^23 + u, so subtracting 2^23 + 128 gives q;
             // |q| < 256 leaves the low 16 bits zero, so the high halves are the bf16 values.
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-              const uint4 v = *reinterpret_cast<const uint4*>(src + (((4 * h + p) ^ sw) << 4));
+              const uint4 v = *reinterpret_cast<const uint4*>(src + (((4 * j + p) ^ sw) << 4));
               const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t wx = w4[j >> 1] ^ 0x80808080u;
-                const uint32_t k0 = (j & 1) * 2;
+              for (int jj = 0; jj < 8; ++jj) {
+                const uint32_t wx = w4[jj >> 1] ^ 0x80808080u;
+                const uint32_t k0 = (jj & 1) * 2;
                 const float q0 = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | k0)) - 8388736.0f;
                 const float q1 = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | (k0 + 1))) - 8388736.0f;
-                o[8 * p + j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632u);
+                o[8 * p + jj] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632u);
+              }
+            }
+          } else if (cvt) {
+            // 64 E2M1 codes (32 bytes), four per 16-bit half word. For each block scale 2^(e - 127)
+            // the eight scaled bf16 values (0 and 0.5, 1, 1.5, 2, 3, 4, 6 times the scale: their
+            // bf16 bits plus (e - 127) << 7, exact for e in 2..252) are split into a table of high
+            // bytes and one of low bytes; each code's 3-bit magnitude selects from both by
+            // byte_perm, the sign goes to the top bit of the high byte, and two more byte_perms
+            // interleave the bytes into bf16 pairs.
+            uint32_t thx[2], thy[2], tlx[2], tly[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int off = static_cast<int>((sc2 >> (8 * hf)) & 0xFFu) - 127;
+              const uint32_t o1 = static_cast<uint32_t>(off) << 7;   // added to one 16-bit value
+              const uint32_t o2 = o1 * 0x10001u;                       // added to both halves
+              const uint32_t A = 0x3F000000u + (o1 << 16);             // values 0 (kept 0) and 0.5
+              const uint32_t Bv = 0x3FC03F80u + o2;                    // 1, 1.5
+              const uint32_t Cv = 0x40404000u + o2;                    // 2, 3
+              const uint32_t Dv = 0x40C04080u + o2;                    // 4, 6
+              thx[hf] = __byte_perm(A, Bv, 0x7531u);
+              tlx[hf] = __byte_perm(A, Bv, 0x6420u);
+              thy[hf] = __byte_perm(Cv, Dv, 0x7531u);
+              tly[hf] = __byte_perm(Cv, Dv, 0x6420u);
+            }
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + (((2 * j + p) ^ sw) << 4));
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {  // 16-bit halves of the piece: four codes each
+                const uint32_t h = w4[jj >> 1] >> (16 * (jj & 1));
+                const uint32_t sel = h & 0x7777u;
+                const uint32_t sgn = __byte_perm(0u, 0x80u, (h >> 1) & 0x4444u);  // 0x80 in byte k if code k < 0
+                const uint32_t hb = __byte_perm(thx[p], thy[p], sel) | sgn;
+                const uint32_t lb = __byte_perm(tlx[p], tly[p], sel);
+                const int oi = 16 * p + 2 * jj;  // output word: elements 2 oi, 2 oi + 1
+                o[oi] = __byte_perm(lb, hb, 0x5140u);
+                o[oi + 1] = __byte_perm(lb, hb, 0x7362u);
               }
             }
           } else {
@@ -797,24 +858,24 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&af_bar[as]);
-            // A slot holding one chunk is read by this group alone: count both groups' arrivals.
-            if (slot_done) mbar_arrive_n(&rawe_bar[r], (!q8i || h == 0) ? 2u : 1u);
-            else mbar_arrive(&rawe_bar[r]);
+            // Release the slot after this warp's last chunk in it; a slot with a single chunk is
+            // read by one group only, which then counts for both.
+            if (c + 2 >= slot_hi) mbar_arrive_n(&rawe_bar[r], slot_hi - slot_lo >= 2 ? 1u : 2u);
           }
         }
         if (++as == C::kASlots) {
           as = 0;
           aphase ^= 1u;
         }
-        if (slot_done && ++r == C::kRawSlots) {
+        if (c + 1 == slot_hi && ++r == C::kRawSlots) {
           r = 0;
           rphase ^= 1u;
         }
       }
     }
   } else {
-    // ---------------- weight-row producer (Q8): the experts' int8 rows (two K chunks per slot) and
-    // the shared MLP's bf16 rows (one K chunk per slot)
+    // ---------------- weight-row producer (Q8): the experts' rows (128 bytes of each per slot: two
+    // int8 or four MXFP4 K chunks) and the shared MLP's bf16 rows (one K chunk per slot)
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     int r = 0;
@@ -829,7 +890,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
       const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const uint64_t pol = it.nt > 2 ? pol_keep : pol_once;
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
-      const int nslots = it.dense ? nch : (nch + 1) / 2;
+      const int nslots = it.dense ? nch : (nch + C::kExpChunksPerSlot - 1) / C::kExpChunksPerSlot;
       for (int sidx = 0; sidx < nslots; ++sidx) {
         if (!warp_wait(&rawe_bar[r], rphase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
@@ -849,7 +910,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
               tma_load_2d(dst, &map_a_d0, &rawf_bar[r], k0, it.m * kBM, pol);
             }
           } else {
-            const int x0 = sidx * 2 * kBK;  // int8: one byte per element
+            const int x0 = sidx * 128;  // 128 bytes of each row: 2 int8 or 4 MXFP4 K chunks
             if (GATE_UP) {
               tma_load_2d(dst, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + it.m * 64, pol);
               tma_load_2d(dst + 64 * 128, &map_q, &rawf_bar[r], x0, it.e * (2 * I) + I + it.m * 64, pol);
@@ -881,17 +942,17 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, Q8>::kThreads, 1)
   }
 }
 
-template <int BN, bool GATE_UP, int MA, bool Q8 = false>
+template <int BN, bool GATE_UP, int MA, int QW = kWBf16>
 cudaError_t launch_t(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s) {
-  using C = Cfg<BN, GATE_UP, MA, Q8>;
-  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP, MA, Q8>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
+  using C = Cfg<BN, GATE_UP, MA, QW>;
+  return launch_pdl(grouped_gemm_kernel<BN, GATE_UP, MA, QW>, dim3(grid), dim3(C::kThreads), C::kSmem, s, m.a_exp,
                     m.a_dense0, m.a_dense1, m.b_exp, m.b_dense, b, T, full_layer, m.a_q, m.q_scale);
 }
 
-template <int BN, bool GATE_UP, int MA, bool Q8 = false>
+template <int BN, bool GATE_UP, int MA, int QW = kWBf16>
 cudaError_t set_limit() {
-  using C = Cfg<BN, GATE_UP, MA, Q8>;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GATE_UP, MA, Q8>,
+  using C = Cfg<BN, GATE_UP, MA, QW>;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GATE_UP, MA, QW>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
 }
 
@@ -915,27 +976,35 @@ cudaError_t gemm_set_smem_limits() {
   if ((e = set_limit<64, false, 1>()) != cudaSuccess) return e;
   if ((e = set_limit<128, false, 1>()) != cudaSuccess) return e;
   if ((e = set_limit<256, false, 1>()) != cudaSuccess) return e;
-  if ((e = set_limit<32, true, 1, true>()) != cudaSuccess) return e;
-  if ((e = set_limit<64, true, 1, true>()) != cudaSuccess) return e;
-  if ((e = set_limit<32, false, 1, true>()) != cudaSuccess) return e;
-  return set_limit<64, false, 1, true>();
+  if ((e = set_limit<32, true, 1, kWInt8>()) != cudaSuccess) return e;
+  if ((e = set_limit<64, true, 1, kWInt8>()) != cudaSuccess) return e;
+  if ((e = set_limit<32, false, 1, kWInt8>()) != cudaSuccess) return e;
+  if ((e = set_limit<64, false, 1, kWInt8>()) != cudaSuccess) return e;
+  if ((e = set_limit<32, true, 1, kWFp4>()) != cudaSuccess) return e;
+  if ((e = set_limit<64, true, 1, kWFp4>()) != cudaSuccess) return e;
+  if ((e = set_limit<32, false, 1, kWFp4>()) != cudaSuccess) return e;
+  return set_limit<64, false, 1, kWFp4>();
 }
 
 // int8 experts (token tiles of 32 or 64): m.a_q is the int8 expert map, m.q_scale the row scales.
-cudaError_t launch_gate_up_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_gate_up_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                               cudaStream_t s) {
-  switch (bn) {
-    case 32: return launch_t<32, true, 1, true>(m, b, T, full_layer, grid, s);
-    case 64: return launch_t<64, true, 1, true>(m, b, T, full_layer, grid, s);
+  switch (bn * 2 + (fp4 ? 1 : 0)) {
+    case 64: return launch_t<32, true, 1, kWInt8>(m, b, T, full_layer, grid, s);
+    case 128: return launch_t<64, true, 1, kWInt8>(m, b, T, full_layer, grid, s);
+    case 65: return launch_t<32, true, 1, kWFp4>(m, b, T, full_layer, grid, s);
+    case 129: return launch_t<64, true, 1, kWFp4>(m, b, T, full_layer, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_down_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_down_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                            cudaStream_t s) {
-  switch (bn) {
-    case 32: return launch_t<32, false, 1, true>(m, b, T, full_layer, grid, s);
-    case 64: return launch_t<64, false, 1, true>(m, b, T, full_layer, grid, s);
+  switch (bn * 2 + (fp4 ? 1 : 0)) {
+    case 64: return launch_t<32, false, 1, kWInt8>(m, b, T, full_layer, grid, s);
+    case 128: return launch_t<64, false, 1, kWInt8>(m, b, T, full_layer, grid, s);
+    case 65: return launch_t<32, false, 1, kWFp4>(m, b, T, full_layer, grid, s);
+    case 129: return launch_t<64, false, 1, kWFp4>(m, b, T, full_layer, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

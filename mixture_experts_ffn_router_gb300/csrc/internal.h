@@ -85,8 +85,8 @@ struct CombineParams {
 // down: a_exp = down rows, a_dense0 = dense down, b_exp = h, b_dense = h_dense (BN-row boxes).
 struct GemmMaps {
   CUtensorMap a_exp, a_dense0, a_dense1, b_exp, b_dense;
-  CUtensorMap a_q;         // int8 expert weights (when the experts are int8)
-  const float* q_scale;    // their row scales
+  CUtensorMap a_q;         // converted expert weights: int8 rows, or packed MXFP4 codes
+  const void* q_scale;     // int8: fp32 row scales; MXFP4: E8M0 block scales [rows, K / 32]
 };
 
 // Launches a kernel with programmatic dependent launch: its CTAs may start while the previous
@@ -143,9 +143,9 @@ cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int 
                         cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
 int gate_up_tiles_per_item(int bn, int T);
-cudaError_t launch_gate_up_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_gate_up_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                               cudaStream_t s);
-cudaError_t launch_down_q8(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_down_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                            cudaStream_t s);
 // SM-pair (cta_group::2) down GEMM for token tiles of 256 (gemm_pair.cu).
 cudaError_t gemm_pair_set_smem_limits();

@@ -183,8 +183,10 @@ struct moe_ffn_ctx {
   const void* cached_dense_down;
   const void* cached_gate_up_q;
   const void* cached_down_q;
+  const void* cached_gate_up_f4;
+  const void* cached_down_f4;
   bool cached_valid;
-  CUtensorMap map_gate_up_q, map_down_q;  // int8 experts
+  CUtensorMap map_gate_up_q, map_down_q;  // converted experts: int8 rows or packed MXFP4 codes
   CUtensorMap map_gate_up, map_down, map_dense_gate, map_dense_up, map_dense_down;
   cudaEvent_t ev_start[kKernelsPerForward];
   cudaEvent_t ev_stop[kKernelsPerForward];
@@ -295,22 +297,33 @@ void moe_ffn_destroy(moe_ffn_ctx* ctx) { delete ctx; }
 
 static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
   const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
-  // int8 experts: all four fields, or none.
+  // int8 experts: all four fields, or none; likewise MXFP4; not both.
   const bool q8 = w->gate_up_q || w->gate_up_scale || w->down_q || w->down_scale;
+  const bool f4 = w->gate_up_f4 || w->gate_up_f4s || w->down_f4 || w->down_f4s;
+  if (q8 && f4) return MOE_FFN_EINVAL;
   if (q8) {
     if (!w->gate_up_q || !w->gate_up_scale || !w->down_q || !w->down_scale) return MOE_FFN_EINVAL;
     if (!aligned16(w->gate_up_q) || !aligned16(w->down_q) || !aligned16(w->gate_up_scale) ||
         !aligned16(w->down_scale))
       return MOE_FFN_EALIGN;
   }
-  if (!w->router_w || !w->router_norm_w || !w->per_expert_scale || (!q8 && (!w->gate_up || !w->down)))
+  if (f4) {
+    if (!w->gate_up_f4 || !w->gate_up_f4s || !w->down_f4 || !w->down_f4s) return MOE_FFN_EINVAL;
+    if (!aligned16(w->gate_up_f4) || !aligned16(w->down_f4) || !aligned16(w->gate_up_f4s) ||
+        !aligned16(w->down_f4s))
+      return MOE_FFN_EALIGN;
+  }
+  const bool cvt = q8 || f4;
+  if (!w->router_w || !w->router_norm_w || !w->per_expert_scale || (!cvt && (!w->gate_up || !w->down)))
     return MOE_FFN_EINVAL;
   if (full && (!w->dense_gate || !w->dense_up || !w->dense_down || !w->pre_ff_ln || !w->pre_ff_ln_2 ||
                !w->post_ff_ln_1 || !w->post_ff_ln_2 || !w->post_ff_ln))
     return MOE_FFN_EINVAL;
-  const void* ps[] = {w->router_w, w->router_norm_w, w->per_expert_scale,
-                      q8 ? static_cast<const void*>(w->gate_up_q) : static_cast<const void*>(w->gate_up),
-                      q8 ? static_cast<const void*>(w->down_q) : static_cast<const void*>(w->down)};
+  const void* gu = f4 ? static_cast<const void*>(w->gate_up_f4)
+                      : q8 ? static_cast<const void*>(w->gate_up_q) : static_cast<const void*>(w->gate_up);
+  const void* dn = f4 ? static_cast<const void*>(w->down_f4)
+                      : q8 ? static_cast<const void*>(w->down_q) : static_cast<const void*>(w->down);
+  const void* ps[] = {w->router_w, w->router_norm_w, w->per_expert_scale, gu, dn};
   for (const void* p : ps)
     if (!aligned16(p)) return MOE_FFN_EALIGN;
   if (full) {
@@ -321,18 +334,21 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
   }
   const bool same = c->cached_gate_up == w->gate_up && c->cached_down == w->down &&
                     c->cached_gate_up_q == w->gate_up_q && c->cached_down_q == w->down_q &&
+                    c->cached_gate_up_f4 == w->gate_up_f4 && c->cached_down_f4 == w->down_f4 &&
                     (!full || (c->cached_dense_gate == w->dense_gate && c->cached_dense_up == w->dense_up &&
                                c->cached_dense_down == w->dense_down));
   if (same && c->cached_valid) return MOE_FFN_OK;
-  // With int8 experts the bf16 expert maps are never read by a kernel; they are encoded over the
-  // int8 arrays (as bf16 of half as many columns) only so that every map handed to a kernel is valid.
-  bool ok = q8 ? encode_u8(&c->map_gate_up_q, w->gate_up_q, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
-                     encode_u8(&c->map_down_q, w->down_q, static_cast<uint64_t>(E) * H, I, 128) &&
-                     encode_bf16(&c->map_gate_up, w->gate_up_q, static_cast<uint64_t>(E) * 2 * I, H / 2, 64) &&
-                     encode_bf16(&c->map_down, w->down_q, static_cast<uint64_t>(E) * H, I / 2, 128)
-               : encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
-                     encode_bf16(&c->map_down, w->down, static_cast<uint64_t>(E) * H, I, 128);
-  if (!q8) {
+  // With converted experts the bf16 expert maps are never read by a kernel; they are encoded over
+  // the converted arrays (as bf16 of fewer columns) only so that every map handed to a kernel is
+  // valid. The converted rows are read as bytes: int8 K bytes per row, MXFP4 K / 2.
+  const uint64_t kb_gu = f4 ? H / 2 : H, kb_dn = f4 ? I / 2 : I;
+  bool ok = cvt ? encode_u8(&c->map_gate_up_q, gu, static_cast<uint64_t>(E) * 2 * I, kb_gu, 64) &&
+                      encode_u8(&c->map_down_q, dn, static_cast<uint64_t>(E) * H, kb_dn, 128) &&
+                      encode_bf16(&c->map_gate_up, gu, static_cast<uint64_t>(E) * 2 * I, kb_gu / 2, 64) &&
+                      encode_bf16(&c->map_down, dn, static_cast<uint64_t>(E) * H, kb_dn / 2, 128)
+                : encode_bf16(&c->map_gate_up, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 64) &&
+                      encode_bf16(&c->map_down, w->down, static_cast<uint64_t>(E) * H, I, 128);
+  if (!cvt) {
     c->map_gate_up_q = c->map_gate_up;
     c->map_down_q = c->map_down;
   }
@@ -352,6 +368,8 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
   c->cached_valid = true;
   c->cached_gate_up_q = w->gate_up_q;
   c->cached_down_q = w->down_q;
+  c->cached_gate_up_f4 = w->gate_up_f4;
+  c->cached_down_f4 = w->down_f4;
   c->cached_gate_up = w->gate_up;
   c->cached_down = w->down;
   c->cached_dense_gate = w->dense_gate;
@@ -391,9 +409,10 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   rp.ks = choose_ks(T);
   rp.tpw = choose_tpw(T);
   // int8 experts run the GEMM variants with an int8 weight ring, built for token tiles of up to 64.
-  const bool q8 = w->gate_up_q != nullptr;
-  // int8 experts: stages are one K chunk each, so a narrow token tile buys pipeline depth; small
-  // batches take 32 tokens, larger ones 64.
+  // Converted experts (int8 or MXFP4) run the GEMM variants with A in tensor memory, built for
+  // token tiles of 32 (small batches, deeper rings) or 64.
+  const bool f4 = w->gate_up_f4 != nullptr;
+  const bool q8 = w->gate_up_q != nullptr || f4;
   rp.bn = q8 ? (T <= 128 ? 32 : 64) : choose_bn(T);
   rp.full_layer = full ? 1 : 0;
   rp.eps = c->cfg.eps;
@@ -423,9 +442,9 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   dn.b_exp = c->map_h[bk];
   dn.b_dense = c->map_hd[bk];
   gu.a_q = c->map_gate_up_q;
-  gu.q_scale = w->gate_up_scale;
+  gu.q_scale = f4 ? static_cast<const void*>(w->gate_up_f4s) : static_cast<const void*>(w->gate_up_scale);
   dn.a_q = c->map_down_q;
-  dn.q_scale = w->down_scale;
+  dn.q_scale = f4 ? static_cast<const void*>(w->down_f4s) : static_cast<const void*>(w->down_scale);
 
   // Persistent GEMM grids: at most one CTA per SM, and no more than an upper bound of the items.
   const int S = T * K;
@@ -457,11 +476,11 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4:
-        e = q8 ? launch_gate_up_q8(bn, gu, c->buf, T, rp.full_layer, grid_gu, s)
+        e = q8 ? launch_gate_up_q8(bn, f4, gu, c->buf, T, rp.full_layer, grid_gu, s)
                : launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s);
         break;
       case 5:
-        e = q8      ? launch_down_q8(bn, dn, c->buf, T, rp.full_layer, grid_dn, s)
+        e = q8      ? launch_down_q8(bn, f4, dn, c->buf, T, rp.full_layer, grid_dn, s)
             : pairs ? launch_down_pair(dn, c->buf, T, rp.full_layer, grid_dn, s)
                     : launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s);
         break;

@@ -1,4 +1,4 @@
-// quant.cu — per-channel symmetric int8 quantisation of expert weights on the device.
+// quant.cu — int8 (per-channel symmetric) and MXFP4 quantisation of expert weights on the device.
 //
 // "Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS Inferentia2 — where every rank weighted the
 // wrong experts", section "Can it run on a smaller box?": the experts are stored as int8 with one
@@ -71,5 +71,85 @@ extern "C" int moe_ffn_quantize_int8(const void* w, long long rows, int cols, in
   moe::quantize_int8_kernel<<<static_cast<unsigned>(blocks), moe::kQuantWarps * 32, 0,
                               static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(w), rows, cols, q,
                                                                    scale);
+  return cudaGetLastError() == cudaSuccess ? MOE_FFN_OK : MOE_FFN_ECUDA;
+}
+
+namespace moe {
+
+namespace {
+
+constexpr int kF4Threads = 256;
+
+// E2M1 magnitude code of a (the element over its block scale, a >= 0): the nearest of 0, 0.5, 1,
+// 1.5, 2, 3, 4, 6 with midpoints going to the even code, magnitudes above 6 saturating to 6.
+__device__ __forceinline__ uint32_t e2m1_magnitude_code(float a) {
+  if (a <= 0.25f) return 0;
+  if (a < 0.75f) return 1;
+  if (a <= 1.25f) return 2;
+  if (a < 1.75f) return 3;
+  if (a <= 2.5f) return 4;
+  if (a < 3.5f) return 5;
+  if (a <= 5.0f) return 6;
+  return 7;
+}
+
+// One thread per block of 32 elements: the block's largest magnitude gives the shared exponent
+// floor(log2 amax) - 2 (ilogbf), every element is scaled by 2^-exponent (exact wherever the
+// rounding decision depends on it) and rounded to E2M1.
+__global__ void __launch_bounds__(kF4Threads)
+    quantize_mxfp4_kernel(const uint16_t* w, long long rows, int cols, uint8_t* codes, uint8_t* scales) {
+  const int nb = cols / 32;
+  const long long blk = static_cast<long long>(blockIdx.x) * kF4Threads + threadIdx.x;
+  if (blk >= rows * nb) return;
+  const long long r = blk / nb;
+  const int b = static_cast<int>(blk - r * nb);
+  const uint16_t* src = w + r * cols + b * 32;
+  float v[32];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint4 q = *reinterpret_cast<const uint4*>(src + 8 * p);
+    const uint32_t q4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * p + 2 * j] = __uint_as_float(q4[j] << 16);
+      v[8 * p + 2 * j + 1] = __uint_as_float(q4[j] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  uint32_t out[4] = {0u, 0u, 0u, 0u};
+  uint8_t sbyte = 0;
+  if (amax > 0.0f) {
+    int se = ilogbf(amax) - 2;
+    se = se < -127 ? -127 : (se > 127 ? 127 : se);
+    sbyte = static_cast<uint8_t>(se + 127);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float a = ldexpf(v[j], -se);
+      uint32_t c = e2m1_magnitude_code(fabsf(a));
+      if (c != 0 && a < 0.0f) c |= 8u;
+      out[j >> 3] |= c << (4 * (j & 7));
+    }
+  }
+  *reinterpret_cast<uint4*>(codes + r * (cols / 2) + b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+  scales[r * nb + b] = sbyte;
+}
+
+}  // namespace
+
+}  // namespace moe
+
+extern "C" int moe_ffn_quantize_mxfp4(const void* w, long long rows, int cols, uint8_t* codes, uint8_t* scales,
+                                      void* stream) {
+  if (!w || !codes || !scales || rows < 0 || cols < 32 || cols % 32 != 0) return MOE_FFN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(w) & 15u) != 0 || (reinterpret_cast<uintptr_t>(codes) & 15u) != 0)
+    return MOE_FFN_EALIGN;
+  if (rows == 0) return MOE_FFN_OK;
+  const long long nblk = rows * (cols / 32);
+  const long long grid = (nblk + moe::kF4Threads - 1) / moe::kF4Threads;
+  if (grid > 0x7FFFFFFFLL) return MOE_FFN_EINVAL;
+  moe::quantize_mxfp4_kernel<<<static_cast<unsigned>(grid), moe::kF4Threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(w), rows, cols, codes, scales);
   return cudaGetLastError() == cudaSuccess ? MOE_FFN_OK : MOE_FFN_ECUDA;
 }
