@@ -107,7 +107,9 @@ typedef struct moe_ffn_weights {
    * weight (row, col) is then e2m1(code) * 2^(scale byte - 127), where the code is the low nibble
    * of byte [row, col / 2] for even col and the high nibble for odd col (bit 3 the sign, bits 2..0
    * index the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) and the scale byte is [row, col / 32] (E8M0).
-   * gate_up / down are not read (the shared MLP stays bf16). moe_ffn_quantize_mxfp4 makes them. */
+   * gate_up / down are not read (the shared MLP stays bf16). moe_ffn_quantize_mxfp4 makes them.
+   * The forward applies a block's scale exactly for scale bytes 2..252 (what the quantiser gives
+   * any block whose largest magnitude is at least 2^-123) and reads all-zero blocks as zero. */
   const uint8_t* gate_up_f4;      /* [128 * 1408, 1408] packed E2M1 codes */
   const uint8_t* gate_up_f4s;     /* [128 * 1408, 88] E8M0 block scales */
   const uint8_t* down_f4;         /* [128 * 2816, 352] packed E2M1 codes */
