@@ -335,8 +335,10 @@ def run_ours(args, wl):
     step(sync_each=count_hits)
     experts_hit = float(np.mean(hits))
 
-    # Breakdown pass (untimed): events around every kernel of each forward, to rank the kernels.
+    # Breakdown pass (untimed): events around every kernel slot of each forward, to rank the
+    # kernels (a slot a forward of this size leaves empty records its two events back to back).
     nk = B.moe_ffn_kernels_per_forward(m.ctx, T)
+    nslots = len(B.KERNEL_NAMES)
     n_b = max(1, min(50, args.steps))
 
     def event_pairs(n):
@@ -348,17 +350,17 @@ def run_ours(args, wl):
 
     # Events go on the last layer's context (every layer runs the same kernels).
     mk = ctxs[-1]
-    bd = [event_pairs(nk) for _ in range(n_b)]
+    bd = [event_pairs(nslots) for _ in range(n_b)]
     torch.cuda.synchronize()
     for i in range(n_b):
-        for k in range(nk):
+        for k in range(nslots):
             B.moe_ffn_set_kernel_events(mk.ctx, k, bd[i][k][0].cuda_event, bd[i][k][1].cuda_event)
         step()
     torch.cuda.synchronize()
-    for k in range(nk):
+    for k in range(nslots):
         B.moe_ffn_set_kernel_events(mk.ctx, k, None, None)
     kernel_us = {B.KERNEL_NAMES[k]: float(np.mean([bd[i][k][0].elapsed_time(bd[i][k][1]) for i in range(n_b)]) * 1e3)
-                 for k in range(nk)}
+                 for k in range(nslots)}
     gemms = {"gate_up_gemm": B.KERNEL_NAMES.index("gate_up_gemm"), "down_gemm": B.KERNEL_NAMES.index("down_gemm")}
     dom = max(gemms, key=lambda n: kernel_us[n])
     dom_k = gemms[dom]

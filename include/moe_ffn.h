@@ -175,10 +175,13 @@ int moe_ffn_device_status(moe_ffn_ctx* ctx, void* stream, uint32_t* word);
 /* Profiling hook: from now on every forward records `start` (a cudaEvent_t as void*) on its stream
  * right before the launch of kernel `kernel` and `stop` right after it. NULL events turn the hook
  * off. kernel: 0 router matrix split, 1 router logits, 2 top-k and pre-norms, 3 permutation,
- * 4 gate_up grouped GEMM, 5 down grouped GEMM, 6 combine and post-norms. */
+ * 4 gate_up grouped GEMM, 5 down grouped GEMM, 6 combine and post-norms. Forwards of at most 64
+ * tokens launch nothing at slot 0 (their router sums run on CUDA cores in slot 1), so its two
+ * events are recorded back to back. */
 int moe_ffn_set_kernel_events(moe_ffn_ctx* ctx, int kernel, void* start, void* stop);
 
-/* Number of kernels one forward of T tokens launches on the device (0 for T = 0). */
+/* Number of kernels one forward of T tokens launches on the device (0 for T = 0; 6 for T <= 64,
+ * else 7). */
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
 
 /* The block's fp32 router logits, [T, 128], for callers that cannot allocate device memory (code

@@ -130,6 +130,9 @@ inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block
 }
 
 constexpr int kKernelsPerForward = 7;
+// Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores (no fold kernel).
+constexpr int kRouterFmaT = 64;
+cudaError_t launch_router_fma(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s);

@@ -406,7 +406,7 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   rp.pre_ff_ln = w->pre_ff_ln;
   rp.pre_ff_ln_2 = w->pre_ff_ln_2;
   rp.T = T;
-  rp.ks = choose_ks(T);
+  rp.ks = T <= kRouterFmaT ? 1 : choose_ks(T);
   rp.tpw = choose_tpw(T);
   // int8 experts run the GEMM variants with an int8 weight ring, built for token tiles of up to 64.
   // Converted experts (int8 or MXFP4) run the GEMM variants with A in tensor memory, built for
@@ -471,8 +471,11 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
     if (c->ev_start[k]) e = cudaEventRecord(c->ev_start[k], s);
     if (e != cudaSuccess) break;
     switch (k) {
-      case 0: e = launch_router_prep(rp, c->buf, s); break;
-      case 1: e = launch_router_logits(c->map_wsplit, rp, c->buf, s); break;
+      // Small batches: no fold kernel, the router's sums on CUDA cores.
+      case 0: e = T <= kRouterFmaT ? cudaSuccess : launch_router_prep(rp, c->buf, s); break;
+      case 1:
+        e = T <= kRouterFmaT ? launch_router_fma(rp, c->buf, s) : launch_router_logits(c->map_wsplit, rp, c->buf, s);
+        break;
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4:
@@ -537,7 +540,7 @@ int moe_ffn_set_kernel_events(moe_ffn_ctx* c, int kernel, void* start, void* sto
 
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* c, int T) {
   if (!c || T < 0) return MOE_FFN_EINVAL;
-  return T == 0 ? 0 : kKernelsPerForward;
+  return T == 0 ? 0 : (T <= kRouterFmaT ? kKernelsPerForward - 1 : kKernelsPerForward);
 }
 
 }  // extern "C"

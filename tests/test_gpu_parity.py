@@ -111,13 +111,16 @@ def test_deterministic_bitwise(T):
 
 def test_context_reuse_across_T_and_weights():
     # One context, calls with different T and different weights: each result equals a fresh run.
+    # The sizes cross between the tensor-core router (T > 64) and the CUDA-core one, and repeat a
+    # decode size, so every per-forward reset of the routing counters is exercised.
     m = B.MoeFFN(FULL, 256)
-    for T, seed in [(256, 800), (17, 801), (130, 802)]:
+    for T, seed in [(256, 800), (17, 801), (130, 802), (64, 803), (64, 804), (1, 805)]:
         x, w = G.make_case(FULL, T, seed)
         a = m.forward(x, w).clone()
         fresh = B.MoeFFN(FULL, T).forward(x, w)
         torch.cuda.synchronize()
         assert torch.equal(a.view(torch.int16), fresh.view(torch.int16))
+    assert m.status() == (B.MOE_FFN_OK, 0)
 
 
 def test_error_paths():
