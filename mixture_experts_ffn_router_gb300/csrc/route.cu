@@ -35,27 +35,11 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Warp arg-max over (logit, expert) pairs: larger logit first, lower expert id on equal logits.
-struct Cand {
-  float l;
-  float p;
-  int e;
-};
-
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  return a.l > b.l || (a.l == b.l && a.e < b.e);
-}
-
-__device__ __forceinline__ Cand warp_argmax(Cand c) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Cand d;
-    d.l = __shfl_xor_sync(0xffffffffu, c.l, o);
-    d.p = __shfl_xor_sync(0xffffffffu, c.p, o);
-    d.e = __shfl_xor_sync(0xffffffffu, c.e, o);
-    if (better(d, c)) c = d;
-  }
-  return c;
+// An unsigned key with the order of the fp32 values (finite; -0 taken as +0), so that a warp
+// maximum of keys is the maximum logit.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -176,22 +160,32 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     int sel_e[K];
     float sel_p[K];
     float l8 = 0.0f, l9 = 0.0f;
+    // Each round: the lane's best untaken logit (the lower j, so the lower id, on equal values),
+    // the warp maximum of their keys, then the lowest expert id among the lanes holding it.
 #pragma unroll
     for (int r = 0; r < K + 1; ++r) {
-      Cand c{-INFINITY, 0.0f, 0x7fffffff};
+      int bj = -1;
+      float bl = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        Cand d{lg[j], pr[j], lane + 32 * j};
-        if (!(taken & (1u << j)) && (c.e == 0x7fffffff || better(d, c))) c = d;
-      }
-      c = warp_argmax(c);
-      if ((c.e & 31) == lane) taken |= 1u << (c.e >> 5);
+      for (int j = 0; j < 4; ++j)
+        if (!(taken & (1u << j)) && (bj < 0 || lg[j] > bl)) {
+          bj = j;
+          bl = lg[j];
+        }
+      const uint32_t key = bj < 0 ? 0u : order_key(bl);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t mine = (bj >= 0 && key == kmax) ? static_cast<uint32_t>(lane + 32 * bj) : 0xffffffffu;
+      const int ew = static_cast<int>(__reduce_min_sync(0xffffffffu, mine));
+      const int wlane = ew & 31, wj = ew >> 5;
+      const float lw = __shfl_sync(0xffffffffu, wj == 0 ? lg[0] : wj == 1 ? lg[1] : wj == 2 ? lg[2] : lg[3], wlane);
+      const float pw = __shfl_sync(0xffffffffu, wj == 0 ? pr[0] : wj == 1 ? pr[1] : wj == 2 ? pr[2] : pr[3], wlane);
+      if (wlane == lane) taken |= 1u << wj;
       if (r < K) {
-        sel_e[r] = c.e;
-        sel_p[r] = c.p;
+        sel_e[r] = ew;
+        sel_p[r] = pw;
       }
-      if (r == K - 1) l8 = c.l;
-      if (r == K) l9 = c.l;
+      if (r == K - 1) l8 = lw;
+      if (r == K) l9 = lw;
     }
     // Ascending expert id (odd-even transposition sort, identical in every lane).
 #pragma unroll
