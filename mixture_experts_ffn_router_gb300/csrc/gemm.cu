@@ -52,46 +52,47 @@ constexpr int kRingBudget = 204800;       // shared memory for the stage ring
 // K chunk of the token tile, which cuts the operand bytes per FLOP from (1/128 + 1/BN) to
 // (1/256 + 1/BN) of the row bytes).
 //
-// Q8: the experts' weights are int8 with one scale per row, and the A operand of every MMA comes
-// from tensor memory. A producer warp streams the weight rows by TMA into a ring of their own
-// (kRawSlots slots of 128 rows x 128 bytes, 128-byte swizzle: two int8 K chunks, or one bf16 K
-// chunk of the shared MLP). Eight converter warps, two groups of four taking alternate K chunks,
-// widen each chunk to bf16 (or copy it) into a ring of kASlots A chunks in TMEM; the stages in
-// shared memory hold only B. The epilogue multiplies the accumulator by the row's scale.
-// QW: the experts' weight format, 0 bf16, 1 int8 (kWInt8), 2 MXFP4 (kWFp4); Q8 = converted weights.
+// QW: the experts' weight format, 0 bf16, 1 int8 (kWInt8), 2 MXFP4 (kWFp4). With a converted
+// format (CVT) the A operand of every MMA comes from tensor memory: a producer warp streams the
+// weight rows by TMA into a ring of their own (kRawSlots slots of 128 rows x 128 bytes, 128-byte
+// swizzle: two int8 K chunks, four MXFP4 K chunks, or one bf16 K chunk of the shared MLP); eight
+// converter warps, two groups of four taking alternate K chunks, widen each chunk to bf16 (or copy
+// it) into a ring of kASlots A chunks in TMEM; the stages in shared memory hold only B; two MMA
+// issuers take alternate K chunks into partial accumulators. int8 rows are scaled in the
+// epilogue (one scale per row), MXFP4 blocks in the widening (one scale per 32 weights).
 constexpr int kWBf16 = 0, kWInt8 = 1, kWFp4 = 2;
 
 template <int BN, bool GATE_UP, int MA, int QW = kWBf16>
 struct Cfg {
-  static constexpr bool Q8 = QW != kWBf16;
+  static constexpr bool CVT = QW != kWBf16;
   static constexpr bool F4 = QW == kWFp4;
-  static constexpr int kExpChunksPerSlot = F4 ? 4 : 2;           // K chunks in a weight-row slot (Q8)
-  static constexpr int KC = (BN <= 64 && !Q8) ? 2 : 1;
-  static constexpr int kAStage = Q8 ? 0 : MA * kAChunk;            // A bytes of one K chunk in a stage
+  static constexpr int kExpChunksPerSlot = F4 ? 4 : 2;           // K chunks in a weight-row slot (CVT)
+  static constexpr int KC = (BN <= 64 && !CVT) ? 2 : 1;
+  static constexpr int kAStage = CVT ? 0 : MA * kAChunk;            // A bytes of one K chunk in a stage
   static constexpr int kBChunk = BN * kBK * 2;
   static constexpr int kChunkBytes = kAStage + kBChunk;
   static constexpr int kStageBytes = KC * kChunkBytes;
-  static constexpr int kRawSlots = Q8 ? (BN <= 32 ? 10 : 8) : 0;   // weight-row ring (Q8)
+  static constexpr int kRawSlots = CVT ? (BN <= 32 ? 10 : 8) : 0;   // weight-row ring (CVT)
   static constexpr int kRawSlotBytes = kBM * 128;                  // 128 rows of 128 bytes
   static constexpr int kStagesRaw = (kRingBudget - kRawSlots * kRawSlotBytes) / kStageBytes;
-  static constexpr int kStageCap = Q8 ? 16 : 8;
+  static constexpr int kStageCap = CVT ? 16 : 8;
   static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
   static constexpr int kEpiWarps = 4 * MA;                         // one per TMEM lane quarter and tile
   static constexpr int kGatherWarps = GATE_UP ? 4 : 0;
   static constexpr int kGatherWarp0 = 2 + kEpiWarps;
-  static constexpr int kConvWarps = Q8 ? 8 : 0;                    // int8 -> bf16 converters
+  static constexpr int kConvWarps = CVT ? 8 : 0;                    // converters to bf16 (CVT)
   static constexpr int kConvWarp0 = kGatherWarp0 + kGatherWarps;
-  static constexpr int kRawWarp = kConvWarp0 + kConvWarps;         // the weight-row producer (Q8)
-  static constexpr int kMma2Warp = kRawWarp + 1;                   // the second MMA issuer (Q8)
-  static constexpr int kIssuers = Q8 ? 2 : 1;
-  static constexpr int kThreads = (kRawWarp + (Q8 ? 2 : 0)) * 32;
+  static constexpr int kRawWarp = kConvWarp0 + kConvWarps;         // the weight-row producer (CVT)
+  static constexpr int kMma2Warp = kRawWarp + 1;                   // the second MMA issuer (CVT)
+  static constexpr int kIssuers = CVT ? 2 : 1;
+  static constexpr int kThreads = (kRawWarp + (CVT ? 2 : 0)) * 32;
   static constexpr int kFullArrivals = 1 + kGatherWarps * 32;
-  static constexpr int kItemConsumers = kIssuers + kEpiWarps + kGatherWarps + kConvWarps + (Q8 ? 1 : 0);
+  static constexpr int kItemConsumers = kIssuers + kEpiWarps + kGatherWarps + kConvWarps + (CVT ? 1 : 0);
   static constexpr int kAccCols = MA * BN;                         // TMEM columns of one accumulator set
   static constexpr int kNAcc = 2 * kAccCols <= 512 ? 2 : 1;        // double-buffered where it fits
-  static constexpr int kACol0 = kNAcc * kIssuers * kAccCols;       // Q8: first TMEM column of the A ring
-  static constexpr int kASlots = Q8 ? (512 - kACol0) / 32 : 0;     // Q8: A chunks (128 x 64 bf16 = 32 columns)
-  static constexpr int kTmemColsRaw = Q8 ? 512 : kNAcc * kAccCols;
+  static constexpr int kACol0 = kNAcc * kIssuers * kAccCols;       // CVT: first TMEM column of the A ring
+  static constexpr int kASlots = CVT ? (512 - kACol0) / 32 : 0;     // CVT: A chunks (128 x 64 bf16 = 32 columns)
+  static constexpr int kTmemColsRaw = CVT ? 512 : kNAcc * kAccCols;
   static constexpr int kTmemCols = kTmemColsRaw < 32 ? 32 : kTmemColsRaw;
   static constexpr int kTilesExp = GATE_UP ? I / 64 : H / kBM;     // 11 | 22 weight tiles per expert
   static constexpr int kTilesDense = GATE_UP ? D / 64 : H / kBM;   // 33 | 22
@@ -101,7 +102,7 @@ struct Cfg {
   static constexpr int kChunksDense = GATE_UP ? H / kBK : D / kBK; // 44 | 33
   // gate_up: the gate/up hand-over [warps][16][32] fp32; down: a 32x32 output chunk per warp.
   static constexpr int kXchgBytes = kEpiWarps * (GATE_UP ? 16 * 32 * 4 : 32 * 32 * 4);
-  static constexpr int kBarBytes = Q8 ? 1024 : 512;
+  static constexpr int kBarBytes = CVT ? 1024 : 512;
   static constexpr int kBarNeed = 8 * (2 * kStages + 5 + 2 * 8 + 2 * kRawSlots + 2 * kASlots) + 8 + 4 * kStages + 4 * 8;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kRawSlots * kRawSlotBytes + kXchgBytes + kBarBytes;
   static_assert(kChunkBytes % 1024 == 0, "operand tiles must stay 1024-byte aligned");
@@ -109,9 +110,9 @@ struct Cfg {
   static_assert(MA == 1 || MA == 2, "MA");
   static_assert(kTmemColsRaw <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(kStages >= 2, "stages");
-  static_assert(!Q8 || (MA == 1 && KC == 1), "int8 weights: one weight tile per item, one K chunk per stage");
-  static_assert(!Q8 || kConvWarps == 8, "two groups of four converter warps, one per TMEM lane quarter");
-  static_assert(!Q8 || kASlots >= 4, "TMEM A ring");
+  static_assert(!CVT || (MA == 1 && KC == 1), "converted weights: one weight tile per item, one K chunk per stage");
+  static_assert(!CVT || kConvWarps == 8, "two groups of four converter warps, one per TMEM lane quarter");
+  static_assert(!CVT || kASlots >= 4, "TMEM A ring");
   static_assert(kBarNeed <= kBarBytes, "barrier area");
   static_assert(kSmem <= 231424, "shared memory");
 };
@@ -235,12 +236,12 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
                         const __grid_constant__ CUtensorMap map_b_dense, Buffers b, int T, int full_layer,
                         const __grid_constant__ CUtensorMap map_q, const void* q_scale) {
   using C = Cfg<BN, GATE_UP, MA, QW>;
-  constexpr bool Q8 = C::Q8;
+  constexpr bool CVT = C::CVT;
   constexpr bool F4 = C::F4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint8_t* raw_ring = smem + C::kStages * C::kStageBytes;  // Q8: weight-row slots
+  uint8_t* raw_ring = smem + C::kStages * C::kStageBytes;  // CVT: weight-row slots
   uint8_t* after_rings = raw_ring + C::kRawSlots * C::kRawSlotBytes;
   float* xchg = reinterpret_cast<float*>(after_rings);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(after_rings + C::kXchgBytes);
@@ -250,10 +251,10 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
   uint64_t* final_bar = acce_bar + 2;
   uint64_t* itemf_bar = final_bar + 1;          // [kItemSlots] item published
   uint64_t* iteme_bar = itemf_bar + kItemSlots; // [kItemSlots] item read by every consumer
-  uint64_t* rawf_bar = iteme_bar + kItemSlots;      // [kRawSlots] Q8: a weight slot has landed
-  uint64_t* rawe_bar = rawf_bar + C::kRawSlots;     // [kRawSlots] Q8: the converters are done with it
-  uint64_t* af_bar = rawe_bar + C::kRawSlots;       // [kASlots] Q8: an A chunk is in TMEM
-  uint64_t* ae_bar = af_bar + C::kASlots;           // [kASlots] Q8: the MMAs are done with it
+  uint64_t* rawf_bar = iteme_bar + kItemSlots;      // [kRawSlots] CVT: a weight slot has landed
+  uint64_t* rawe_bar = rawf_bar + C::kRawSlots;     // [kRawSlots] CVT: the converters are done with it
+  uint64_t* af_bar = rawe_bar + C::kRawSlots;       // [kASlots] CVT: an A chunk is in TMEM
+  uint64_t* ae_bar = af_bar + C::kASlots;           // [kASlots] CVT: the MMAs are done with it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ae_bar + C::kASlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* width_s = reinterpret_cast<int*>(tmem_slot + 2);  // [kStages] MMA width of each stage
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     fence_barrier_init();
     prefetch_tmap(&map_a_exp);
     if (!GATE_UP) prefetch_tmap(&map_b_exp);
-    if (Q8) prefetch_tmap(&map_q);
+    if (CVT) prefetch_tmap(&map_q);
     if (full_layer) {
       prefetch_tmap(&map_a_d0);
       if (GATE_UP) prefetch_tmap(&map_a_d1);
@@ -361,8 +362,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       // gate_up with two tiles: tile 0 holds the gate rows and tile 1 the up rows of 128 features
       // ("paired"); otherwise each tile holds the gate and up rows of 64 features ("stacked").
       const bool paired = GATE_UP && MA == 2 && na == 2;
-      // Q8: every A chunk reaches tensor memory through the converter warps, not by TMA.
-      const bool a_tma = !Q8;
+      // Converted weights: every A chunk reaches tensor memory through the converter warps, not by TMA.
+      const bool a_tma = !CVT;
       for (int c0 = 0; c0 < nch; c0 += C::KC) {
         if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
@@ -426,8 +427,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       for (int s2 = 0; s2 < C::kStages; ++s2)
         if (armed & (1u << s2)) mbar_wait_timeout(&full_bar[s2], (armed_par >> s2) & 1u, kSpinLimitNs, b.status);
     __syncwarp();
-  } else if (warp == 1 || (Q8 && warp == C::kMma2Warp)) {
-    // ---------------- MMA issuer (one thread; Q8: two, issuer j taking the item's K chunks with
+  } else if (warp == 1 || (CVT && warp == C::kMma2Warp)) {
+    // ---------------- MMA issuer (one thread; CVT: two, issuer j taking the item's K chunks with
     // index parity j, each into its own partial accumulator, which the epilogue adds in that order)
     if (lane == 0) {
       const int mi = warp == 1 ? 0 : 1;
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      int aslot = 0;  // Q8: TMEM A ring
+      int aslot = 0;  // CVT: TMEM A ring
       uint32_t aphase = 0;
       bool ok = true;
       int slot = 0;
@@ -458,13 +459,13 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
               ok = false;
               break;
             }
-            if (Q8 && !mbar_wait_bounded(&af_bar[aslot], aphase, abort_flag, b.status, kStatusWaitFull)) {
+            if (CVT && !mbar_wait_bounded(&af_bar[aslot], aphase, abort_flag, b.status, kStatusWaitFull)) {
               ok = false;
               break;
             }
             // The gathered B rows were written by cp.async (generic proxy); the MMA reads them
             // through the async proxy.
-            if (GATE_UP || Q8) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (GATE_UP || CVT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_after();
             // The MMA is only as wide as the tile's token rows (rounded up to the MMA's step of 16).
             if (first) {
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
             const uint32_t st = smem_u32(stages + stage * C::kStageBytes);
             for (int cc = 0; cc < nck; ++cc) {
               const uint64_t b_desc = smem_desc_sw128(st + cc * C::kChunkBytes + C::kAStage);
-              if constexpr (Q8) {
+              if constexpr (CVT) {
                 const uint32_t a_tm = tmem_base + static_cast<uint32_t>(C::kACol0 + aslot * 32);
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k)
@@ -495,9 +496,9 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
             }
             first = false;
             umma_commit(&empty_bar[stage]);
-            if (Q8) umma_commit(&ae_bar[aslot]);
+            if (CVT) umma_commit(&ae_bar[aslot]);
           }
-          if (Q8 && ++aslot == C::kASlots) {
+          if (CVT && ++aslot == C::kASlots) {
             aslot = 0;
             aphase ^= 1u;
           }
@@ -570,9 +571,9 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * C::kIssuers * C::kAccCols + ta * BN);
-      // Q8: this lane's weight row's scale (gate_up: lanes 0..63 gate rows, 64..127 up rows).
+      // CVT: this lane's weight row's scale (gate_up: lanes 0..63 gate rows, 64..127 up rows).
       float row_scale = 1.0f;
-      if (Q8 && !F4 && !it.dense && has_tile) {
+      if (CVT && !F4 && !it.dense && has_tile) {
         const size_t row = GATE_UP ? static_cast<size_t>(it.e) * (2 * I) + (q < 2 ? 0 : I) + tile * 64 + 32 * (q & 1) + lane
                                    : static_cast<size_t>(it.e) * H + tile * kBM + 32 * q + lane;
         row_scale = __ldg(static_cast<const float*>(q_scale) + row);
@@ -582,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
         if (paired || !has_tile || c * 32 >= it.rows) break;
         float v[32];
         tmem_ld32(t_row + c * 32, v);
-        if (Q8) {
+        if (CVT) {
           // The second issuer's partial sum (the item's odd K chunks), added in a fixed order.
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
@@ -739,7 +740,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     }
     cp_async_wait_all();
   } else if (warp < C::kRawWarp) {
-    // ---------------- converters (Q8): weight rows from the raw ring into the TMEM A ring. Group g
+    // ---------------- converters (CVT): weight rows from the raw ring into the TMEM A ring. Group g
     // (warps 4g..4g+3 of the eight) takes the item's K chunks with index parity g, so two chunks are
     // in flight; each warp covers the TMEM lane quarter it may access (warp % 4), one weight row per
     // lane, the chunk's 64 K elements per row. A raw slot holds cps chunks of every row (int8 2,
@@ -874,7 +875,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       }
     }
   } else {
-    // ---------------- weight-row producer (Q8): the experts' rows (128 bytes of each per slot: two
+    // ---------------- weight-row producer (CVT): the experts' rows (128 bytes of each per slot: two
     // int8 or four MXFP4 K chunks) and the shared MLP's bf16 rows (one K chunk per slot)
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
@@ -986,8 +987,9 @@ cudaError_t gemm_set_smem_limits() {
   return set_limit<64, false, 1, kWFp4>();
 }
 
-// int8 experts (token tiles of 32 or 64): m.a_q is the int8 expert map, m.q_scale the row scales.
-cudaError_t launch_gate_up_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+// Converted experts (token tiles of 32 or 64): m.a_q maps the int8 rows or MXFP4 codes, m.q_scale holds
+// the int8 row scales or the MXFP4 block scales.
+cudaError_t launch_gate_up_cvt(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                               cudaStream_t s) {
   switch (bn * 2 + (fp4 ? 1 : 0)) {
     case 64: return launch_t<32, true, 1, kWInt8>(m, b, T, full_layer, grid, s);
@@ -998,7 +1000,7 @@ cudaError_t launch_gate_up_q8(int bn, bool fp4, const GemmMaps& m, const Buffers
   }
 }
 
-cudaError_t launch_down_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_down_cvt(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                            cudaStream_t s) {
   switch (bn * 2 + (fp4 ? 1 : 0)) {
     case 64: return launch_t<32, false, 1, kWInt8>(m, b, T, full_layer, grid, s);

@@ -146,9 +146,9 @@ cudaError_t launch_down(int bn, const GemmMaps& m, const Buffers& b, int T, int 
                         cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
 int gate_up_tiles_per_item(int bn, int T);
-cudaError_t launch_gate_up_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_gate_up_cvt(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                               cudaStream_t s);
-cudaError_t launch_down_q8(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
+cudaError_t launch_down_cvt(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                            cudaStream_t s);
 // SM-pair (cta_group::2) down GEMM for token tiles of 256 (gemm_pair.cu).
 cudaError_t gemm_pair_set_smem_limits();

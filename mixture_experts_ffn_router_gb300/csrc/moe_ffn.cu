@@ -408,12 +408,11 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   rp.T = T;
   rp.ks = T <= kRouterFmaT ? 1 : choose_ks(T);
   rp.tpw = choose_tpw(T);
-  // int8 experts run the GEMM variants with an int8 weight ring, built for token tiles of up to 64.
   // Converted experts (int8 or MXFP4) run the GEMM variants with A in tensor memory, built for
   // token tiles of 32 (small batches, deeper rings) or 64.
   const bool f4 = w->gate_up_f4 != nullptr;
-  const bool q8 = w->gate_up_q != nullptr || f4;
-  rp.bn = q8 ? (T <= 128 ? 32 : 64) : choose_bn(T);
+  const bool cvt = w->gate_up_q != nullptr || f4;
+  rp.bn = cvt ? (T <= 128 ? 32 : 64) : choose_bn(T);
   rp.full_layer = full ? 1 : 0;
   rp.eps = c->cfg.eps;
   rp.router_scale = c->cfg.router_scale;
@@ -451,7 +450,7 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   const int bn = rp.bn;
   const int ub_tiles = (S < E ? S : E) + S / bn;
   const int nd = full ? (T + bn - 1) / bn : 0;
-  const int ma = q8 ? 1 : gate_up_tiles_per_item(bn, T);
+  const int ma = cvt ? 1 : gate_up_tiles_per_item(bn, T);
   const long items_gu = static_cast<long>(ub_tiles) * ((I / 64 + ma - 1) / ma) +
                         static_cast<long>(nd) * ((D / 64 + ma - 1) / ma);
   const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
@@ -459,7 +458,7 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
   // For token tiles of 256 (T above 1024) the down GEMM runs on SM pairs: M = 256 per pair of
   // CTAs, half of each token tile in each CTA, so its B maps are the ones with 128-row boxes.
-  const bool pairs = bn == 256 && c->pair_clusters > 0 && !q8;
+  const bool pairs = bn == 256 && c->pair_clusters > 0 && !cvt;
   if (pairs) {
     grid_dn = 2 * c->pair_clusters;
     dn.b_exp = c->map_h[2];
@@ -479,11 +478,11 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4:
-        e = q8 ? launch_gate_up_q8(bn, f4, gu, c->buf, T, rp.full_layer, grid_gu, s)
+        e = cvt ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, rp.full_layer, grid_gu, s)
                : launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s);
         break;
       case 5:
-        e = q8      ? launch_down_q8(bn, f4, dn, c->buf, T, rp.full_layer, grid_dn, s)
+        e = cvt     ? launch_down_cvt(bn, f4, dn, c->buf, T, rp.full_layer, grid_dn, s)
             : pairs ? launch_down_pair(dn, c->buf, T, rp.full_layer, grid_dn, s)
                     : launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s);
         break;

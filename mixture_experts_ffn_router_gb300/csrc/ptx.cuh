@@ -1,4 +1,4 @@
-// ptx.cuh — inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled and gather4), tcgen05
+// ptx.cuh — inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled), tcgen05
 // (TMEM alloc, MMA, commit, load) and PDL. Every wait is bounded: after kSpinLimitNs of waiting it
 // gives up, records the reason in the global status word and returns false, so a kernel whose
 // producer died never hangs the GPU.
@@ -149,18 +149,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Loads four rows r0..r3 (one-row box of the map) starting at inner coordinate c0 into four
-// consecutive rows of shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int r0,
-                                            int r1, int r2, int r3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)),
-      "l"(policy)
       : "memory");
 }
 
