@@ -392,7 +392,7 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
 // One CTA per token, 8 features per thread. Every load that does not depend on another is issued
 // before the first use: the token's 8 slot positions, then its 8 rows of y, d and x, so the CTA
 // waits for memory about twice (positions, then rows) rather than once per load.
-__global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(CombineParams p, Buffers b) {
+__global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(CombineParams p, Buffers b) {
   __shared__ float2 red[kCombineThreads / 32];
   const int t = blockIdx.x, tid = threadIdx.x;
   const int f = tid * 8;
