@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   // TMEM) has completed and every arrival on the other CTA's barriers has been made.
   tc_fence_before();
   __syncthreads();
+  // The combine launches when this GEMM ends (its CTAs waiting beside the GEMM slowed it).
   pdl_launch_dependents();
   cluster_sync_all();
   if (warp == 1) {

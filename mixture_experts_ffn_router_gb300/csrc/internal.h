@@ -132,6 +132,8 @@ inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block
 constexpr int kKernelsPerForward = 7;
 // Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores (no fold kernel).
 constexpr int kRouterFmaT = 64;
+// Largest batch for which the down GEMM lets the combine kernel launch before it ends.
+constexpr int kEarlyCombineT = 64;
 cudaError_t launch_router_fma(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s);

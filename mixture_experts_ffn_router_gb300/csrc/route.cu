@@ -43,20 +43,40 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 }
 
 // ------------------------------------------------------------------------------------------
-// K2: one warp per token. RMS of x; the two pre-norms (full layer) or a copy of x (experts
-// only) as the expert input; logits = rms * scale * sum of the partials; fp32 softmax; top-8 by
-// logit with the 9th for the gap; renormalise, times per_expert_scale; slots listed in ascending
-// expert id. Each CTA counts its slots per expert; the last CTA to finish turns the counts into
-// expert offsets, per-CTA base positions and the grouped GEMMs' token-tile list.
+// K2: one warp per token. RMS of x; logits = rms * scale * sum of the partials; fp32 softmax;
+// top-8 by logit with the 9th for the gap; renormalise, times per_expert_scale; slots listed in
+// ascending expert id. Each CTA counts its slots per expert and takes a finish ticket, then writes
+// its tokens' expert-branch inputs (the two pre-norms in the full layer, else a copy of x); the
+// last CTA to finish turns the counts into expert offsets, per-CTA base positions and the grouped
+// GEMMs' token-tile list.
 __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffers b) {
   __shared__ int hist_s[E];
   __shared__ int part_s[2][E];
   __shared__ int scan_s[E + 1];
   __shared__ int tscan_s[E + 1];
+  __shared__ float pes_s[E];
+  // 1 + pre_feedforward_layernorm and 1 + pre_feedforward_layernorm_2 (full layer), so that the
+  // norm loop below reads no global memory between its stores.
+  __shared__ __align__(16) float g_s[2][H];
+  __shared__ float inv_s[kScatterTok];  // 1 / RMS of the CTA's tokens (8 tpw <= 256)
   __shared__ int is_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < E) hist_s[tid] = 0;
+  // Weights only, so they may be read before the wait for the router's partial sums: this grid
+  // starts only after every router CTA has passed its own wait, so all earlier work on the
+  // stream is complete. L2-coherent loads, so no line cached by an earlier kernel is seen.
+  if (tid < E) pes_s[tid] = __ldcg(p.per_expert_scale + tid);
+  if (p.full_layer)
+    for (int i = tid; i < H / 4; i += 256) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(p.pre_ff_ln) + i);
+      const float4 c = __ldcg(reinterpret_cast<const float4*>(p.pre_ff_ln_2) + i);
+      reinterpret_cast<float4*>(g_s[0])[i] = make_float4(1.0f + a.x, 1.0f + a.y, 1.0f + a.z, 1.0f + a.w);
+      reinterpret_cast<float4*>(g_s[1])[i] = make_float4(1.0f + c.x, 1.0f + c.y, 1.0f + c.z, 1.0f + c.w);
+    }
   pdl_wait();
+  // Dependents may launch now: they run nothing before their own wait that reads this grid's
+  // results, and everything before this grid is complete.
+  pdl_launch_dependents();
   __syncthreads();
 
   const int tb = 8 * p.tpw;
@@ -68,7 +88,7 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     {
       uint4 xv[11];
 #pragma unroll
-      for (int c = 0; c < 11; ++c) xv[c] = xr[lane + 32 * c];
+      for (int c = 0; c < 11; ++c) xv[c] = __ldg(xr + lane + 32 * c);
 #pragma unroll
       for (int c = 0; c < 11; ++c) {
         const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
@@ -83,61 +103,27 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     ss = warp_sum(ss);
     const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + p.eps);
 
-    // Expert-branch input n2 and dense-branch input n1.
-    uint4* n2r = reinterpret_cast<uint4*>(b.n2 + static_cast<size_t>(t) * H);
-    if (p.full_layer) {
-      uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
-#pragma unroll
-      for (int c = 0; c < 11; ++c) {
-        // x again (an L1 hit: this warp read the row just above), so that the row does not stay in
-        // registers and the kernel keeps four CTAs per SM.
-        const uint4 xc = xr[lane + 32 * c];
-        const int col = (lane + 32 * c) * 8;
-        const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
-        const float4 a0 = *reinterpret_cast<const float4*>(p.pre_ff_ln + col);
-        const float4 a1 = *reinterpret_cast<const float4*>(p.pre_ff_ln + col + 4);
-        const float4 c0 = *reinterpret_cast<const float4*>(p.pre_ff_ln_2 + col);
-        const float4 c1 = *reinterpret_cast<const float4*>(p.pre_ff_ln_2 + col + 4);
-        const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float g2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t o1[4], o2[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
-          o1[j] = pack_bf16(lo * (1.0f + g1[2 * j]), hi * (1.0f + g1[2 * j + 1]));
-          o2[j] = pack_bf16(lo * (1.0f + g2[2 * j]), hi * (1.0f + g2[2 * j + 1]));
-        }
-        n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-        n2r[lane + 32 * c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = xr[lane + 32 * c];
-    }
+    if (lane == 0) inv_s[warp * p.tpw + i] = inv;
 
-    // Logits: expert e = lane + 32 j, partial sums added in ascending split order.
-    // Partial sums of the 4 experts of this lane, added in ascending split order, with 32 loads
-    // in flight at a time.
+    // Logits: expert e = lane + 32 j. The partial sums of the lane's 4 experts are added in
+    // ascending split order, loaded 8 splits (32 loads) at a time, the last group predicated.
     float lg[4], pr[4];
     {
       const float* pp = b.logits_part + static_cast<size_t>(t) * E + lane;
       const size_t stride = static_cast<size_t>(p.T) * E;
       float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      int s = 0;
-      for (; s + 8 <= p.ks; s += 8) {
+      for (int s = 0; s < p.ks; s += 8) {
         float a[8][4];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) a[u][j] = pp[(s + u) * stride + 32 * j];
+          for (int j = 0; j < 4; ++j) a[u][j] = s + u < p.ks ? pp[(s + u) * stride + 32 * j] : 0.0f;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) z[j] += a[u][j];
+          for (int j = 0; j < 4; ++j)
+            if (s + u < p.ks) z[j] += a[u][j];
       }
-      for (; s < p.ks; ++s)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) z[j] += pp[s * stride + 32 * j];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         lg[j] = z[j] * inv * p.router_scale;
@@ -214,7 +200,7 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
           e = sel_e[j];
           pp = sel_p[j];
         }
-      const float w = (pp / psum) * p.per_expert_scale[e];
+      const float w = (pp / psum) * pes_s[e];
       b.topk_idx[static_cast<size_t>(t) * K + lane] = e;
       b.topk_w[static_cast<size_t>(t) * K + lane] = w;
       atomicAdd(&hist_s[e], 1);
@@ -233,84 +219,151 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     const int ticket = atomicAdd(b.done_ctr, 1);
     is_last = (ticket == static_cast<int>(gridDim.x) - 1);
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
 
-  const int nb = (p.T + kScatterTok - 1) / kScatterTok;  // chunks
-  const int e = tid & (E - 1), half = tid >> 7;
-  const int bmid = (nb + 1) / 2;
-  const int blo = half ? bmid : 0, bhi = half ? nb : bmid;
-  {
-    int s = 0;
-    for (int bb = blo; bb < bhi; ++bb) s += __ldcg(b.hist + bb * E + e);
-    part_s[half][e] = s;
-  }
   __syncthreads();
-  if (warp == 0) {
-    // Exclusive scans over the 128 experts of the counts and of the token-tile counts.
-    int cnt[4], nt[4];
-    int cs = 0, ts = 0;
+  // The last CTA builds the schedule first, so that it does not wait behind its own row stores.
+  if (is_last) {
+    __threadfence();
+
+    const int nb = (p.T + kScatterTok - 1) / kScatterTok;  // chunks
+    const int e = tid & (E - 1), half = tid >> 7;
+    const int bmid = (nb + 1) / 2;
+    const int blo = half ? bmid : 0, bhi = half ? nb : bmid;
+    // Eight chunks' counts in flight at a time; the first eight stay in registers for the base
+    // positions below (all of them up to T = 4096).
+    int c8[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int ee = lane * 4 + j;
-      cnt[j] = part_s[0][ee] + part_s[1][ee];
-      nt[j] = (cnt[j] + p.bn - 1) / p.bn;
-      cs += cnt[j];
-      ts += nt[j];
+    for (int u = 0; u < 8; ++u) c8[u] = blo + u < bhi ? __ldcg(b.hist + (blo + u) * E + e) : 0;
+    {
+      int s = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s += c8[u];
+      for (int b0 = blo + 8; b0 < bhi; b0 += 8) {
+        int d8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) d8[u] = b0 + u < bhi ? __ldcg(b.hist + (b0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += d8[u];
+      }
+      part_s[half][e] = s;
     }
-    int ci = cs, ti = ts;
+    __syncthreads();
+    if (warp == 0) {
+      // Exclusive scans over the 128 experts of the counts and of the token-tile counts.
+      int cnt[4], nt[4];
+      int cs = 0, ts = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, ci, o);
-      const int c = __shfl_up_sync(0xffffffffu, ti, o);
-      if (lane >= o) {
-        ci += a;
-        ti += c;
+      for (int j = 0; j < 4; ++j) {
+        const int ee = lane * 4 + j;
+        cnt[j] = part_s[0][ee] + part_s[1][ee];
+        nt[j] = (cnt[j] + p.bn - 1) / p.bn;
+        cs += cnt[j];
+        ts += nt[j];
+      }
+      int ci = cs, ti = ts;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ci, o);
+        const int c = __shfl_up_sync(0xffffffffu, ti, o);
+        if (lane >= o) {
+          ci += a;
+          ti += c;
+        }
+      }
+      int cex = ci - cs, tex = ti - ts;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int ee = lane * 4 + j;
+        scan_s[ee] = cex;
+        tscan_s[ee] = tex;
+        b.counts[ee] = cnt[j];
+        b.offsets[ee] = cex;
+        b.tile_off[ee] = tex;
+        cex += cnt[j];
+        tex += nt[j];
+      }
+      if (lane == 31) {
+        scan_s[E] = cex;
+        tscan_s[E] = tex;
+        b.offsets[E] = cex;
+        b.tile_off[E] = tex;
+        if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
+        *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
+        b.sched[0] = 0;  // the GEMMs of this forward claim their work items from these counters
+        b.sched[1] = 0;
       }
     }
-    int cex = ci - cs, tex = ti - ts;
+    __syncthreads();
+    {
+      // Base position of each (CTA, expert): the expert's offset plus the slots of earlier CTAs.
+      int run = scan_s[e] + (half ? part_s[0][e] : 0);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int ee = lane * 4 + j;
-      scan_s[ee] = cex;
-      tscan_s[ee] = tex;
-      b.counts[ee] = cnt[j];
-      b.offsets[ee] = cex;
-      b.tile_off[ee] = tex;
-      cex += cnt[j];
-      tex += nt[j];
+      for (int u = 0; u < 8; ++u)
+        if (blo + u < bhi) {
+          b.base[(blo + u) * E + e] = run;
+          run += c8[u];
+        }
+      for (int b0 = blo + 8; b0 < bhi; b0 += 8) {
+        int d8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) d8[u] = b0 + u < bhi ? __ldcg(b.hist + (b0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (b0 + u < bhi) {
+            b.base[(b0 + u) * E + e] = run;
+            run += d8[u];
+          }
+      }
     }
-    if (lane == 31) {
-      scan_s[E] = cex;
-      tscan_s[E] = tex;
-      b.offsets[E] = cex;
-      b.tile_off[E] = tex;
-      if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
-      *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
-      b.sched[0] = 0;  // the GEMMs of this forward claim their work items from these counters
-      b.sched[1] = 0;
-    }
-  }
-  __syncthreads();
-  {
-    // Base position of each (CTA, expert): the expert's offset plus the slots of earlier CTAs.
-    int run = scan_s[e] + (half ? part_s[0][e] : 0);
-    for (int bb = blo; bb < bhi; ++bb) {
-      const int c = __ldcg(b.hist + bb * E + e);
-      b.base[bb * E + e] = run;
-      run += c;
+    if (half == 0 && tscan_s[E] <= b.max_tiles) {
+      const int cnt = scan_s[e + 1] - scan_s[e];
+      const int nt = tscan_s[e + 1] - tscan_s[e];
+      for (int j = 0; j < nt; ++j) {
+        const int rows = min(p.bn, cnt - j * p.bn);
+        b.exp_tiles[tscan_s[e] + j] = make_int4(e, scan_s[e] + j * p.bn, rows, 0);
+      }
     }
   }
-  if (half == 0 && tscan_s[E] <= b.max_tiles) {
-    const int cnt = scan_s[e + 1] - scan_s[e];
-    const int nt = tscan_s[e + 1] - tscan_s[e];
-    for (int j = 0; j < nt; ++j) {
-      const int rows = min(p.bn, cnt - j * p.bn);
-      b.exp_tiles[tscan_s[e] + j] = make_int4(e, scan_s[e] + j * p.bn, rows, 0);
+
+  // The normalised rows are written only now: the routing above never waits behind these stores
+  // (46 MB at T = 4096), and the last CTA's scan above overlaps the other CTAs' writes.
+  for (int i = 0; i < p.tpw; ++i) {
+    const int t = blockIdx.x * tb + warp * p.tpw + i;
+    if (t >= p.T) break;
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
+    const float inv = inv_s[warp * p.tpw + i];
+    // Expert-branch input n2 and dense-branch input n1.
+    uint4* n2r = reinterpret_cast<uint4*>(b.n2 + static_cast<size_t>(t) * H);
+    if (p.full_layer) {
+      uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
+#pragma unroll
+      for (int c = 0; c < 11; ++c) {
+        const int col = (lane + 32 * c) * 8;
+        const float4 a0 = *reinterpret_cast<const float4*>(&g_s[0][col]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&g_s[0][col + 4]);
+        const float4 c0 = *reinterpret_cast<const float4*>(&g_s[1][col]);
+        const float4 c1 = *reinterpret_cast<const float4*>(&g_s[1][col + 4]);
+        const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float g2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        // x again, read-only (this warp read the row above), so the row does not stay in
+        // registers; the weights come from shared memory, so no load waits for a store.
+        const uint4 xc = __ldg(xr + lane + 32 * c);
+        const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
+        uint32_t o1[4], o2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
+          o1[j] = pack_bf16(lo * g1[2 * j], hi * g1[2 * j + 1]);
+          o2[j] = pack_bf16(lo * g2[2 * j], hi * g2[2 * j + 1]);
+        }
+        n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        n2r[lane + 32 * c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = __ldg(xr + lane + 32 * c);
     }
   }
-  pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -323,6 +376,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteParams p, Buffe
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 8 * E; i += 256) (&mask_s[0][0])[i] = 0u;
   pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   const int t = blockIdx.x * kScatterTok + warp * 32 + lane;
   const bool valid = t < p.T;
@@ -397,6 +451,7 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(CombinePara
   const int t = blockIdx.x, tid = threadIdx.x;
   const int f = tid * 8;
   pdl_wait();
+  pdl_launch_dependents();
   const int4 pa = *reinterpret_cast<const int4*>(b.slot_pos + static_cast<size_t>(t) * K);
   const int4 pb = *reinterpret_cast<const int4*>(b.slot_pos + static_cast<size_t>(t) * K + 4);
   float dv[8];
