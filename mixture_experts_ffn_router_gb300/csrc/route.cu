@@ -56,8 +56,11 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
   __shared__ int tscan_s[E + 1];
   __shared__ float pes_s[E];
   // 1 + pre_feedforward_layernorm and 1 + pre_feedforward_layernorm_2 (full layer), so that the
-  // norm loop below reads no global memory between its stores.
-  __shared__ __align__(16) float g_s[2][H];
+  // norm loop below reads no global memory between its stores. Column group q = lane + 32 c (8
+  // columns) is stored as two float4 halves at g_s[v][c][half][lane]: a warp's 16-byte loads
+  // then hit consecutive addresses (a plain [H] layout puts lanes 32 bytes apart, two-way bank
+  // conflicts).
+  __shared__ float4 g_s[2][11][2][32];
   __shared__ float inv_s[kScatterTok];  // 1 / RMS of the CTA's tokens (8 tpw <= 256)
   __shared__ int is_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -70,8 +73,9 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     for (int i = tid; i < H / 4; i += 256) {
       const float4 a = __ldcg(reinterpret_cast<const float4*>(p.pre_ff_ln) + i);
       const float4 c = __ldcg(reinterpret_cast<const float4*>(p.pre_ff_ln_2) + i);
-      reinterpret_cast<float4*>(g_s[0])[i] = make_float4(1.0f + a.x, 1.0f + a.y, 1.0f + a.z, 1.0f + a.w);
-      reinterpret_cast<float4*>(g_s[1])[i] = make_float4(1.0f + c.x, 1.0f + c.y, 1.0f + c.z, 1.0f + c.w);
+      const int q = i >> 1, hf = i & 1;  // float4 i holds columns 4i..4i+3 of group q
+      g_s[0][q >> 5][hf][q & 31] = make_float4(1.0f + a.x, 1.0f + a.y, 1.0f + a.z, 1.0f + a.w);
+      g_s[1][q >> 5][hf][q & 31] = make_float4(1.0f + c.x, 1.0f + c.y, 1.0f + c.z, 1.0f + c.w);
     }
   pdl_wait();
   // Dependents may launch now: they run nothing before their own wait that reads this grid's
@@ -338,11 +342,8 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
       uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
 #pragma unroll
       for (int c = 0; c < 11; ++c) {
-        const int col = (lane + 32 * c) * 8;
-        const float4 a0 = *reinterpret_cast<const float4*>(&g_s[0][col]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&g_s[0][col + 4]);
-        const float4 c0 = *reinterpret_cast<const float4*>(&g_s[1][col]);
-        const float4 c1 = *reinterpret_cast<const float4*>(&g_s[1][col + 4]);
+        const float4 a0 = g_s[0][c][0][lane], a1 = g_s[0][c][1][lane];
+        const float4 c0 = g_s[1][c][0][lane], c1 = g_s[1][c][1][lane];
         const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         const float g2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         // x again, read-only (this warp read the row above), so the row does not stay in

@@ -286,7 +286,9 @@ constexpr int kRouterFmaTok = 16;  // tokens per CTA: two per warp
 constexpr int kRouterFmaExp = 4;   // experts per CTA
 
 __global__ void __launch_bounds__(kRouterFmaThreads) router_fma_kernel(RouteParams p, Buffers b) {
-  __shared__ float4 wp[kRouterFmaExp][H / 4];
+  // W' of expert ee, column group q (8 columns) as two float4 halves at wp[ee][half][q], so that
+  // lanes reading groups q = lane + 32 k hit consecutive 16-byte words (no bank conflicts).
+  __shared__ float4 wp[kRouterFmaExp][2][H / 8];
   const int e0 = blockIdx.x * kRouterFmaExp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(kRouterFmaThreads) router_fma_kernel(RoutePara
 #pragma unroll
     for (int ee = 0; ee < kRouterFmaExp; ++ee) {
       const float4 w = reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e0 + ee) * H)[i];
-      wp[ee][i] = make_float4(w.x * (1.0f + g.x), w.y * (1.0f + g.y), w.z * (1.0f + g.z), w.w * (1.0f + g.w));
+      wp[ee][i & 1][i >> 1] = make_float4(w.x * (1.0f + g.x), w.y * (1.0f + g.y), w.z * (1.0f + g.z), w.w * (1.0f + g.w));
     }
   }
   __syncthreads();
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(kRouterFmaThreads) router_fma_kernel(RoutePara
   for (int k = 0; k < 11; ++k) {
 #pragma unroll
     for (int ee = 0; ee < kRouterFmaExp; ++ee) {
-      const float4 w0 = wp[ee][2 * (lane + 32 * k)], w1 = wp[ee][2 * (lane + 32 * k) + 1];
+      const float4 w0 = wp[ee][0][lane + 32 * k], w1 = wp[ee][1][lane + 32 * k];
       const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
