@@ -16,7 +16,8 @@
 //     accumulator, and the chunk sums are added in fp32 registers, so the tensor core's own
 //     accumulation spans only the 192 products of one chunk.
 // MMA: M = 128 experts (A = a W' part, K-major, by TMA), N = 128 tokens (B = x rows, K-major,
-// staged by the producer warp). Warp 0 loads, warp 1 issues the MMAs, warps 2..5 add chunk sums.
+// staged by the producer warp). Warp 0 loads, warp 1 issues the MMAs, warps 2..9 add chunk sums
+// (two per TMEM lane quarter, half of the token columns each).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -26,7 +27,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreadsR = 192;
+constexpr int kThreadsR = 320;
 constexpr int kTile = 128 * 64 * 2;              // one 128-row x 64-element bf16 tile, 16 KB
 constexpr int kStagesR = 3;
 constexpr int kAccR = 4;                         // rotating chunk accumulators in TMEM
@@ -79,6 +80,17 @@ __global__ void __launch_bounds__(kPrepThreads) router_prep_kernel(RouteParams p
   dst[2 * part] = make_uint4(pack2(lo[0], lo[1]), pack2(lo[2], lo[3]), pack2(lo[4], lo[5]), pack2(lo[6], lo[7]));
 }
 
+// Orders the reads of registers filled by tcgen05.ld after tcgen05.wait::ld: the empty asm
+// "rewrites" them, so no use can be scheduled between the load and the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     }
     for (int a = 0; a < kAccR; ++a) {
       mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], 4);
+      mbar_init(&acce_bar[a], 8);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -136,7 +148,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   pdl_launch_dependents();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *b.done_ctr = 0;
   // The per-chunk expert counts that the top-k kernel accumulates start from zero.
-  if (blockIdx.y == 0 && threadIdx.x >= 64)
+  if (blockIdx.y == 0 && threadIdx.x >= 64 && threadIdx.x < 64 + E)
     for (int c = blockIdx.x; c < (p.T + kScatterTok - 1) / kScatterTok; c += gridDim.x)
       b.hist[c * E + threadIdx.x - 64] = 0;
 
@@ -216,11 +228,15 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- warps 2..5: add the chunk sums (TMEM lane = expert) in fp32
+    // ---------------- warps 2..9: add the chunk sums (TMEM lane = expert) in fp32. The two warps of
+    // a lane quarter take half of the N token columns each, with all their TMEM loads of a chunk
+    // in flight before one wait (one dependent wait per chunk instead of N / 32).
     const int q = warp & 3;
-    float z[N];
+    const int hf = (warp - 2) >> 2;
+    constexpr int NH = N / 2;
+    float z[NH];
 #pragma unroll
-    for (int j = 0; j < N; ++j) z[j] = 0.0f;
+    for (int j = 0; j < NH; ++j) z[j] = 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -232,12 +248,16 @@ __global__ void __launch_bounds__(kThreadsR, 1)
         break;
       }
       tc_fence_after();
+      uint32_t r[NH / 32][32];
 #pragma unroll
-      for (int g = 0; g < N / 32; ++g) {
-        float v[32];
-        tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * N + g * 32, v);
+      for (int g = 0; g < NH / 32; ++g)
+        tmem_ld32_nowait(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * N + hf * NH + g * 32, r[g]);
+      tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[g * 32 + j] += v[j];
+      for (int g = 0; g < NH / 32; ++g) {
+        reg_fence32(r[g]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[g * 32 + j] += __uint_as_float(r[g][j]);
       }
       tc_fence_before();
       __syncwarp();
@@ -250,8 +270,8 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     if (ok) {
       const int e = q * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
-        const int t = t0 + j;
+      for (int j = 0; j < NH; ++j) {
+        const int t = t0 + hf * NH + j;
         if (t < p.T) b.logits_part[(static_cast<size_t>(ks) * p.T + t) * E + e] = z[j];
       }
     }
