@@ -561,6 +561,8 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
           tmem_ld32_nowait(t_g + c * 32, g);
           tmem_ld32_nowait(t_g + BN + c * 32, u);
           tmem_wait_ld();
+          reg_fence32(g);
+          reg_fence32(u);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             hs[j * 32 + lane] = f32_to_bf16_rn(gelu_tanh_approx(__uint_as_float(g[j])) * __uint_as_float(u[j]));
