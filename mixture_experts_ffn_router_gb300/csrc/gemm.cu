@@ -326,7 +326,9 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     // ---------------- producer: TMA loads of A, and of B when its rows are contiguous
     // Weight tiles that at least two more token tiles of the same group read again are kept in L2
     // (evict_last); the rest stream through (evict_first). Keeping tiles with one re-read was
-    // measured slower: the lines stay protected in L2 long after their last use.
+    // measured slower: the lines stay protected in L2 long after their last use. So was keeping
+    // the shared MLP's tiles at 64-token tiles (T <= 256: up to four token tiles, read at nearly
+    // the same time anyway): the 30-layer stack at T = 256 took 8.51 vs 8.23 ms.
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_x = pol_keep;
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       const int width = min(BN, (it.rows + 15) & ~15);
       const int n_tiles_raw = it.dense ? C::kTilesDense : C::kTilesExp;
       const int na = min(MA, n_tiles_raw - it.m * MA);  // weight tiles of this item
-      const uint64_t pol_w = it.nt > 2 ? pol_keep : pol_once;
+      const uint64_t pol_w = (it.nt > 2 && !(it.dense && BN <= 64)) ? pol_keep : pol_once;
       // gate_up with two tiles: tile 0 holds the gate rows and tile 1 the up rows of 128 features
       // ("paired"); otherwise each tile holds the gate and up rows of 64 features ("stacked").
       const bool paired = GATE_UP && MA == 2 && na == 2;

@@ -94,13 +94,13 @@ int choose_tpw(int T) {
   return 1;
 }
 
-// Token tile of the bf16 GEMMs: 64 tokens with two K chunks per stage up to T = 128 (at T = 128
-// gate_up 159 vs 172 us with 128-token tiles). Above that the shared MLP would have four or more
-// token tiles and its weights would be kept in L2 (evict_last), which slowed the 30-layer stack,
-// so 128 up to 1024 (two weight tiles per gate_up item above 512), then 256.
+// Token tile of the bf16 GEMMs: 64 tokens with two K chunks per stage up to T = 256 (more weight
+// bytes in flight per SM than 128-token tiles: at T = 128 gate_up 159 vs 172 us; layer at T = 256
+// 278.1 vs 283.6 us, the 30-layer stack 8.23 vs 8.48 ms), 128 up to 1024 (two weight tiles per
+// gate_up item above 512), then 256.
 int choose_bn(int T) {
   if (T <= 32) return 32;
-  if (T <= 128) return 64;
+  if (T <= 256) return 64;
   if (T <= 1024) return 128;
   return 256;
 }
