@@ -28,8 +28,8 @@ METRIC = "MoE-FFN tokens/s at T=64 & T=4096; % of HBM or bf16 TC roofline"
 UNIT = "tokens/s"
 H, E, K, I, D = 2816, 128, 8, 704, 2112
 
-# Algorithmic bytes per unit: one expert's gate_up and down slices, the shared
-# MLP's matrices, the router matrix.
+# Algorithmic bytes per unit: one expert's gate_up and down slices, the shared MLP's matrices and
+# the router matrix, each read once per forward.
 GATE_UP_BYTES_PER_EXPERT = 2 * I * H * 2        # 7,929,856
 DOWN_BYTES_PER_EXPERT = H * I * 2               # 3,964,928
 DENSE_GATE_UP_BYTES = 2 * D * H * 2             # 23,789,568

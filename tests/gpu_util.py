@@ -1,7 +1,7 @@
 """Helpers shared by the GPU parity tests: run the CUDA path through the C ABI, run the oracle on
 the same drawn tensors, and compare them under the block's acceptance rules.
 
-Rules (the spec acceptance of the block):
+Rules (the block's acceptance bar):
   * expert choice (the set of 8) bit-exact on every token whose 8th/9th oracle-logit gap > 1e-4;
     on the other tokens any choice is accepted whose experts all lie within 1e-4 of the oracle's
     8th logit (several answers are correct there);
