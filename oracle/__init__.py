@@ -21,8 +21,11 @@ Pins (what the oracle is checked against, in ``tests/test_oracle_pins.py``):
     lands in [4, 8) scale units), exact grid values, the per-interval error bound and saturation,
     ties to the even code, symmetry, zero blocks; the layer with MXFP4 experts against brute.py on
     the dequantised weights.
+  * The pins themselves: ``tests/test_oracle_mutants.py`` plants one plausible mistake at a time in
+    a copy of ``moe_oracle.c`` and requires the pin files to fail on each.
 """
 import ctypes
+import os
 
 import numpy as np
 
@@ -95,10 +98,15 @@ class Outputs(ctypes.Structure):
 
 
 def lib():
-    """Loads (building first if needed) the oracle's shared library."""
+    """Loads (building first if needed) the oracle's shared library.
+
+    MOE_ORACLE_LIB, when set, names another build of the same C source to load instead: the
+    mutation test (tests/test_oracle_mutants.py) points it at copies with one planted mistake each
+    and checks that the pins then fail.
+    """
     global _LIB
     if _LIB is None:
-        path = _build.build()
+        path = os.environ.get("MOE_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         L.moe_oracle_gelu_tanh.restype = ctypes.c_double
         L.moe_oracle_gelu_tanh.argtypes = [ctypes.c_double]

@@ -336,8 +336,8 @@ int moe_oracle_route(const moe_oracle_dims* d, int T, const uint16_t* x, const m
   return bad ? -1 : 0;
 }
 
-/* Slots sorted by (expert, token): the gather that precedes each expert's MLP and the scatter
- * back ([MoE] "The architecture": the experts' sparse gather/scatter loop), as a counting sort. */
+/* Per-channel symmetric int8 ([MoE] "Can it run on a smaller box?"): one fp32 scale per row,
+ * max|w| / 127; each element w / scale rounded to nearest (ties to even) and clamped to ±127. */
 int moe_oracle_quantize_int8(const uint16_t* w, long long rows, int cols, int8_t* q, float* scale) {
   if (!w || !q || !scale || rows < 0 || cols < 1) return -1;
   for (long long r = 0; r < rows; ++r) {
@@ -376,6 +376,9 @@ static int e2m1_code(double v) {
   return (best != 0 && v < 0) ? (best | 8) : best;
 }
 
+/* MXFP4 ([MoE] "The fp4 rabbit hole": 32 fp4 values share one scale), read as the OCP
+ * Microscaling v1.0 conversion: per block of 32 consecutive elements of a row, a power-of-two
+ * scale from the block's largest magnitude, then every element rounded to E2M1. */
 int moe_oracle_quantize_mxfp4(const uint16_t* w, long long rows, int cols, uint8_t* codes, uint8_t* scales) {
   if (!w || !codes || !scales || rows < 0 || cols < 32 || cols % 32 != 0) return -1;
   const int nb = cols / 32;
@@ -414,6 +417,8 @@ int moe_oracle_quantize_mxfp4(const uint16_t* w, long long rows, int cols, uint8
   return 0;
 }
 
+/* Slots sorted by (expert, token): the gather that precedes each expert's MLP and the scatter
+ * back ([MoE] "The architecture": the experts' sparse gather/scatter loop), as a counting sort. */
 int moe_oracle_permute(int T, int K, int E, const int32_t* topk_idx, const float* topk_w,
                        int32_t* counts, int32_t* offsets, int32_t* perm, float* w_sorted,
                        int32_t* slot_pos) {
