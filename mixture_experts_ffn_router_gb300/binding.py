@@ -208,19 +208,70 @@ def moe_ffn_destroy(ctx: int) -> None:
 
 # ------------------------------------------------------------------ torch convenience layer
 
+def _field_specs():
+    """Element type and element count of every weight field, as include/moe_ffn.h states them."""
+    import torch
+    H, E, K2, I, D = HIDDEN, N_EXPERTS, 2 * MOE_INTER, MOE_INTER, DENSE_INTER
+    f32, bf16, i8, u8 = torch.float32, torch.bfloat16, torch.int8, torch.uint8
+    spec = {"router_w": (f32, E * H), "router_norm_w": (f32, H), "per_expert_scale": (f32, E),
+            "gate_up": (bf16, E * K2 * H), "down": (bf16, E * H * I), "dense_gate": (bf16, D * H),
+            "dense_up": (bf16, D * H), "dense_down": (bf16, H * D),
+            "gate_up_q": (i8, E * K2 * H), "gate_up_scale": (f32, E * K2), "down_q": (i8, E * H * I),
+            "down_scale": (f32, E * H), "gate_up_f4": (u8, E * K2 * H // 2), "gate_up_f4s": (u8, E * K2 * H // 32),
+            "down_f4": (u8, E * H * I // 2), "down_f4s": (u8, E * H * I // 32)}
+    for name in ("pre_ff_ln", "pre_ff_ln_2", "post_ff_ln_1", "post_ff_ln_2", "post_ff_ln"):
+        spec[name] = (f32, H)
+    return spec
+
+
+def _check_type_size(what, t, dtype, numel):
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if t.numel() != numel:
+        raise ValueError("%s must hold %d elements, got %d" % (what, numel, t.numel()))
+
+
+def _check_placement(what, t):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % what)
+
+
 def weights_struct(w: dict) -> moe_ffn_weights:
-    """A moe_ffn_weights whose fields point at the CUDA tensors of ``w`` (absent fields are NULL)."""
+    """A moe_ffn_weights whose fields point at the CUDA tensors of ``w`` (absent fields are NULL).
+
+    Each present tensor must have the field's element type and element count (include/moe_ffn.h),
+    so that the kernels never read past a tensor that is too small. Types and sizes of all fields
+    are checked before any placement, so a wrong one is named first."""
+    spec = _field_specs()
+    present = [(f, w[f]) for f in WEIGHT_FIELDS + INT8_FIELDS + F4_FIELDS if w.get(f) is not None]
+    for f, t in present:
+        _check_type_size("weight " + f, t, *spec[f])
     s = moe_ffn_weights()
-    for f in WEIGHT_FIELDS + INT8_FIELDS + F4_FIELDS:
-        t = w.get(f)
-        if t is not None:
-            if not t.is_cuda or not t.is_contiguous():
-                raise ValueError("weight %s must be a contiguous CUDA tensor" % f)
-            setattr(s, f, t.data_ptr())
+    for f, t in present:
+        _check_placement("weight " + f, t)
+        setattr(s, f, t.data_ptr())
     if "layer_scalar" not in w:
         raise ValueError("layer_scalar is required")
     s.layer_scalar = float(w["layer_scalar"])
     return s
+
+
+def check_io(x, out=None) -> int:
+    """Checks a forward's input (and output, if given): contiguous bf16 CUDA tensors of shape
+    [T, 2816], the output the same shape as the input. Returns T."""
+    import torch
+    if x.dim() != 2 or x.shape[1] != HIDDEN:
+        raise ValueError("x must have shape [T, %d], got %s" % (HIDDEN, tuple(x.shape)))
+    T = x.shape[0]
+    _check_type_size("x", x, torch.bfloat16, T * HIDDEN)
+    if out is not None:
+        if tuple(out.shape) != tuple(x.shape):
+            raise ValueError("out must have the shape of x %s, got %s" % (tuple(x.shape), tuple(out.shape)))
+        _check_type_size("out", out, torch.bfloat16, T * HIDDEN)
+    _check_placement("x", x)
+    if out is not None:
+        _check_placement("out", out)
+    return T
 
 
 class MoeFFN:
@@ -242,7 +293,7 @@ class MoeFFN:
 
     def forward(self, x, weights, out=None, stream=None):
         import torch
-        T = x.shape[0]
+        T = check_io(x, out)
         if out is None:
             out = torch.empty_like(x)
         ws = weights if isinstance(weights, moe_ffn_weights) else weights_struct(weights)
