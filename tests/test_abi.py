@@ -89,3 +89,60 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="not built"):
         B.lib()
+
+
+C_CALLER = r"""
+#include <stdint.h>
+#include <stdio.h>
+#include "moe_ffn.h"
+
+int main(void) {
+  moe_ffn_config c = {MOE_FFN_HIDDEN, MOE_FFN_N_EXPERTS, MOE_FFN_TOP_K, MOE_FFN_MOE_INTER,
+                      MOE_FFN_DENSE_INTER, MOE_FFN_FULL_LAYER, 64, 1e-6f, 0.018844459f};
+  void* fake = (void*)(uintptr_t)4096; /* never dereferenced: every call below fails its checks first */
+  printf("bytes %zu\n", moe_ffn_workspace_bytes(&c));
+  printf("kernels %d\n", moe_ffn_kernels_per_forward(NULL, 4));
+  printf("noalloc_toobig %d\n", moe_ffn_router_logits_noalloc(fake, 1025, fake, fake, 0.02f, 1e-6f, fake, NULL));
+  printf("noalloc_align %d\n",
+         moe_ffn_router_logits_noalloc((void*)(uintptr_t)4098, 4, fake, fake, 0.02f, 1e-6f, fake, NULL));
+  printf("int8_cols %d\n", moe_ffn_quantize_int8(fake, 4, 7, fake, fake, NULL));
+  printf("fp4_cols %d\n", moe_ffn_quantize_mxfp4(fake, 4, 48, fake, fake, NULL));
+#ifdef WITH_INIT
+  moe_ffn_ctx* ctx = (moe_ffn_ctx*)fake;
+  int rc = moe_ffn_init(&ctx, &c, fake, moe_ffn_workspace_bytes(&c), 0);
+  printf("init %d %d\n", rc, ctx == NULL);
+  moe_ffn_destroy(ctx);
+#endif
+  printf("status %s\n", moe_ffn_status_string(MOE_FFN_ETOOBIG));
+  return 0;
+}
+"""
+
+
+def test_plain_c_caller_links_the_library(lib, tmp_path):
+    # A C11 program, built with warnings as errors, includes the header and links the shared
+    # library with no Python in between; the calls it makes fail their argument checks with the
+    # header's status codes before any device work.
+    import torch
+    src = tmp_path / "caller.c"
+    exe = tmp_path / "caller"
+    src.write_text(C_CALLER)
+    pkg = os.path.dirname(B.LIB_PATH)
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+           str(src), "-L", pkg, "-lmoe_ffn", "-Wl,-rpath," + pkg, "-o", str(exe)]
+    if not torch.cuda.is_available():
+        cmd.insert(1, "-DWITH_INIT")
+    subprocess.run(cmd, check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, timeout=120).stdout
+    got = dict(l.split(" ", 1) for l in out.strip().split("\n"))
+    assert int(got["bytes"]) == B.moe_ffn_workspace_bytes(B.make_config(B.MOE_FFN_FULL_LAYER, 64))
+    assert int(got["kernels"]) == B.MOE_FFN_EINVAL
+    assert int(got["noalloc_toobig"]) == B.MOE_FFN_ETOOBIG
+    assert int(got["noalloc_align"]) == B.MOE_FFN_EALIGN
+    assert int(got["int8_cols"]) == B.MOE_FFN_EINVAL
+    assert int(got["fp4_cols"]) == B.MOE_FFN_EINVAL
+    assert got["status"] == B.moe_ffn_status_string(B.MOE_FFN_ETOOBIG)
+    if "init" in got:
+        # No usable sm_103 device here: init reports a CUDA or architecture error and leaves NULL.
+        rc, is_null = map(int, got["init"].split())
+        assert rc in (B.MOE_FFN_ECUDA, B.MOE_FFN_EARCH) and is_null == 1
