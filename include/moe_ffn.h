@@ -225,6 +225,23 @@ int moe_ffn_quantize_int8(const void* w, long long rows, int cols, int8_t* q, fl
 int moe_ffn_quantize_mxfp4(const void* w, long long rows, int cols, uint8_t* codes, uint8_t* scales,
                            void* stream);
 
+/* Self-test of the bounded device waits behind MOE_FFN_EDEVICE (failure detection); the pages have
+ * no counterpart. Queues on `stream` one kernel of one CTA that waits on an mbarrier nothing
+ * arrives on, through the same helpers the forward's kernels wait with:
+ *   wait 1, bounded: gives up after the 2 s limit, ORs 0x1 (a wait for a filled stage gave up)
+ *           into *status_word and raises the CTA's abort flag;
+ *   wait 2, bounded: leaves at once through the abort flag and sets nothing (its bit, 0x2, stays
+ *           clear);
+ *   wait 3, exit drain with a 1 ms limit: gives up and ORs 0x40.
+ * Nothing faults, traps or hangs; the kernel ends after about 2 s and the context stays usable.
+ *   status_word  device pointer to one uint32 the caller has zeroed;
+ *   record       device pointer to 6 uint64: record[2i] = nanoseconds wait i+1 took,
+ *                record[2i+1] = 1 if its phase completed (0 expected for all three);
+ *   stream       cudaStream_t as void*; the host is not synchronised.
+ * Runs on the calling thread's current device. Returns MOE_FFN_EINVAL for a NULL pointer,
+ * MOE_FFN_EARCH on a device other than sm_103, MOE_FFN_ECUDA if the launch fails. */
+int moe_ffn_selftest_wait_expiry(uint32_t* status_word, unsigned long long* record, void* stream);
+
 /* A static string naming a status code. */
 const char* moe_ffn_status_string(int status);
 

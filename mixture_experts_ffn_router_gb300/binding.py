@@ -82,6 +82,8 @@ def lib():
         L.moe_ffn_router_logits_noalloc.restype = ctypes.c_int
         L.moe_ffn_router_logits_noalloc.argtypes = [_vp, ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                                      _vp, _vp]
+        L.moe_ffn_selftest_wait_expiry.restype = ctypes.c_int
+        L.moe_ffn_selftest_wait_expiry.argtypes = [_vp, _vp, _vp]
         L.moe_ffn_status_string.restype = ctypes.c_char_p
         L.moe_ffn_status_string.argtypes = [ctypes.c_int]
         L.moe_ffn_quantize_int8.restype = ctypes.c_int
@@ -159,6 +161,10 @@ def moe_ffn_router_logits_noalloc(x: int, T: int, router_w: int, router_norm_w: 
     cannot allocate); its scratch is a fixed array shared by all calls, see include/moe_ffn.h."""
     return lib().moe_ffn_router_logits_noalloc(_vp(x), int(T), _vp(router_w), _vp(router_norm_w),
                                                float(router_scale), float(eps), _vp(logits), _vp(stream))
+
+
+def moe_ffn_selftest_wait_expiry(status_word: int, record: int, stream: int) -> int:
+    return lib().moe_ffn_selftest_wait_expiry(_vp(status_word), _vp(record), _vp(stream))
 
 
 def moe_ffn_quantize_int8(w: int, rows: int, cols: int, q: int, scale: int, stream: int) -> int:

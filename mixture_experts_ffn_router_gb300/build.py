@@ -13,7 +13,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_ffn.so")
-SOURCES = ["moe_ffn.cu", "route.cu", "router.cu", "gemm.cu", "gemm_pair.cu", "quant.cu", "noalloc.cu"]
+SOURCES = ["moe_ffn.cu", "route.cu", "router.cu", "gemm.cu", "gemm_pair.cu", "quant.cu", "noalloc.cu",
+           "selftest.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
