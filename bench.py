@@ -38,6 +38,26 @@ ROUTER_BYTES = E * H * 4                        # 1,441,792
 FLOPS_PER_TOKEN_EXPERTS = K * 2 * (2 * I * H + H * I)   # 95,158,272
 FLOPS_PER_TOKEN_DENSE = 2 * (2 * D * H + H * D)         # 35,684,352
 
+# Nominal GB300 peaks, for context beside the measured ones: the ~8 TB/s HBM3e figure decode is
+# quoted against, and the dense bf16 tensor rate.
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def layer_roofline(layer_bytes, layer_flops, step_s, hbm_gbs, bf16_tflops, experts_hit, layers):
+    """The whole layer's roofline time max(bytes / HBM, FLOPs / bf16 peak) and the fraction of it a
+    measured per-layer step reaches: `frac` against the measured peaks passed in, `frac_nominal`
+    against the nominal ones."""
+    t_hbm, t_tc = layer_bytes / (hbm_gbs * 1e9), layer_flops / (bf16_tflops * 1e12)
+    t_roof = max(t_hbm, t_tc)
+    t_nom = max(layer_bytes / (NOMINAL_HBM_GBS * 1e9), layer_flops / (NOMINAL_BF16_TFLOPS * 1e12))
+    return {"bytes": layer_bytes, "flops": layer_flops, "roofline_us": t_roof * 1e6, "step_us": step_s * 1e6,
+            "frac": t_roof / step_s, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_nominal_us": t_nom * 1e6, "frac_nominal": t_nom / step_s,
+            "nominal_peaks": {"hbm_gbs": NOMINAL_HBM_GBS, "bf16_tflops": NOMINAL_BF16_TFLOPS},
+            "experts_hit": experts_hit, "layers_per_step": layers}
+
+
 WORKLOADS = {
     "decode64": dict(full=True, T=64, skew=False,
                      desc="Gemma-4 26B-A4B full dual-path FFN layer, decode batch T=64, uniform routing"),
@@ -446,11 +466,8 @@ def run_ours(args, wl):
     layer_bytes = experts_hit * (gu_pe + dn_pe) + ROUTER_BYTES + T * H * 2 * 2 \
         + ((DENSE_GATE_UP_BYTES + DENSE_DOWN_BYTES) if full else 0)
     layer_flops = T * (FLOPS_PER_TOKEN_EXPERTS + (FLOPS_PER_TOKEN_DENSE if full else 0))
-    t_roof = max(layer_bytes / (hbm * 1e9), layer_flops / (tc_burst * 1e12))
     step_s = ms / args.steps / 1e3 / L  # per layer
-    layer = {"bytes": layer_bytes, "flops": layer_flops, "roofline_us": t_roof * 1e6, "step_us": step_s * 1e6,
-             "frac": t_roof / step_s, "bound": "hbm" if layer_bytes / (hbm * 1e9) >= layer_flops / (tc_burst * 1e12) else "tensor",
-             "experts_hit": experts_hit, "layers_per_step": L}
+    layer = layer_roofline(layer_bytes, layer_flops, step_s, hbm, tc_burst, experts_hit, L)
 
     # ---- end to end through the public API with host buffers. Every step copies its whole input
     # from pinned host memory and its whole output back. As in a serving loop, the copies run on two

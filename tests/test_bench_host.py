@@ -1,0 +1,56 @@
+"""Host-side arithmetic of bench.py (CPU only): the algorithmic byte and FLOP counts per unit follow
+from the block's shapes, and the layer roofline reproduces hand-computed figures for the decode
+and prefill workloads against the measured and the nominal peaks."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+H, E, K, I, D = 2816, 128, 8, 704, 2112
+EXPERT_BYTES = 3 * I * H * 2            # gate, up and down of one expert, bf16: 11,894,784
+DENSE_BYTES = 3 * D * H * 2             # the shared MLP's three matrices: 35,684,352
+
+
+def test_unit_counts_follow_from_the_shapes():
+    assert bench.GATE_UP_BYTES_PER_EXPERT + bench.DOWN_BYTES_PER_EXPERT == EXPERT_BYTES == 11_894_784
+    assert bench.DENSE_GATE_UP_BYTES + bench.DENSE_DOWN_BYTES == DENSE_BYTES == 35_684_352
+    assert bench.ROUTER_BYTES == E * H * 4
+    # Two FLOPs per multiply-add: per token, K experts of gate+up (2I x H) and down (H x I), and the
+    # shared MLP's gate+up (2D x H) and down (H x D).
+    assert bench.FLOPS_PER_TOKEN_EXPERTS + bench.FLOPS_PER_TOKEN_DENSE == 130_842_624
+
+
+def _layer(T, experts_hit, step_us):
+    b = experts_hit * EXPERT_BYTES + DENSE_BYTES + E * H * 4 + T * H * 2 * 2
+    f = T * 130_842_624
+    return bench.layer_roofline(b, f, step_us * 1e-6, 6794.5, 1916.3, experts_hit, 1)
+
+
+def test_decode_roofline_is_the_weight_stream():
+    # T=64 with 127 experts hit: 1,548,484,608 bytes, 227.9 us at 6794.5 GB/s, 193.6 us at 8 TB/s.
+    r = _layer(64, 127, 253.1)
+    assert r["bytes"] == 1_548_484_608 and r["bound"] == "hbm"
+    assert r["roofline_us"] == pytest.approx(1_548_484_608 / 6794.5e3, rel=1e-12)
+    assert r["roofline_us"] == pytest.approx(227.9, abs=0.05)
+    assert r["roofline_nominal_us"] == pytest.approx(193.56, abs=0.01)
+    assert r["frac"] == pytest.approx(227.9 / 253.1, abs=1e-3)
+    assert r["frac_nominal"] == pytest.approx(193.56 / 253.1, abs=1e-3)
+
+
+def test_prefill_roofline_is_the_tensor_rate():
+    # T=4096: 535.9 GFLOP, 279.7 us at 1916.3 TFLOP/s, 238.2 us at 2.25 PFLOP/s; the bytes (88
+    # experts hit) take far less.
+    r = _layer(4096, 88, 592.7)
+    assert r["flops"] == 4096 * 130_842_624 and r["bound"] == "tensor"
+    assert r["roofline_us"] == pytest.approx(279.7, abs=0.05)
+    assert r["roofline_nominal_us"] == pytest.approx(238.19, abs=0.01)
+    assert r["frac"] == pytest.approx(279.7 / 592.7, abs=1e-3)
+
+
+def test_job_throughput_counts_every_rank():
+    assert bench.job_throughput(64, 10, 1, 0.5) == pytest.approx(1280.0)
+    assert bench.job_throughput(64, 10, 4, 0.5) == pytest.approx(5120.0)
