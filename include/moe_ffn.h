@@ -152,7 +152,11 @@ size_t moe_ffn_workspace_bytes(const moe_ffn_config* cfg);
 int moe_ffn_init(moe_ffn_ctx** ctx, const moe_ffn_config* cfg, void* workspace,
                  size_t workspace_bytes, int device);
 
-/* Queues one forward of the block on `stream`: out = block(x) for T tokens.
+/* Queues one forward of the block on `stream`: out = block(x) for T tokens, the block being the
+ * dual-path layer of "Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS Inferentia2", section "The
+ * architecture: a dual-path FFN nobody warned me about" (described at the top of this file). Each
+ * expert multiplies only the tokens routed to it; the result equals the post's "compute all
+ * experts, mask to top-8" form (section "The traceable trick") up to rounding.
  *   x   device pointer, [T, 2816] bf16, the layer input (the post-attention residual).
  *   T   0..max_tokens; T = 0 queues nothing and returns MOE_FFN_OK.
  *   w   host pointer to a weights struct whose fields are device pointers; the struct is read
@@ -205,16 +209,17 @@ int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
 int moe_ffn_router_logits_noalloc(const void* x, int T, const float* router_w, const float* router_norm_w,
                                   float router_scale, float eps, float* logits, void* stream);
 
-/* Per-channel symmetric int8 quantisation of a bf16 matrix [rows, cols] on the device, one channel
- * per row: scale[r] = max_c |w[r, c]| / 127 in fp32, q[r, c] = w[r, c] / scale[r] in fp32 rounded
+/* Per-channel symmetric int8 quantisation of a bf16 matrix [rows, cols] on the device (the int8
+ * experts of the 26B-A4B post, section "Can it run on a smaller box?"), one channel per row: scale[r] = max_c |w[r, c]| / 127 in fp32, q[r, c] = w[r, c] / scale[r] in fp32 rounded
  * to nearest (ties to even) and clamped to [-127, 127]; an all-zero row gets scale 0 and q 0. All
  * pointers are device pointers; w and q 16-byte aligned, cols a multiple of 8. Asynchronous on
  * `stream`. Returns MOE_FFN_EINVAL / MOE_FFN_EALIGN on bad arguments, MOE_FFN_ECUDA if the launch
  * fails. */
 int moe_ffn_quantize_int8(const void* w, long long rows, int cols, int8_t* q, float* scale, void* stream);
 
-/* MXFP4 quantisation of a bf16 matrix [rows, cols] on the device, after the OCP Microscaling
- * Formats (MX) v1.0 conversion: for each block of 32 consecutive elements of a row, amax = max |w|;
+/* MXFP4 quantisation of a bf16 matrix [rows, cols] on the device (the microscaling fp4 experts of
+ * the 26B-A4B post, section "The fp4 rabbit hole"), after the OCP Microscaling Formats (MX) v1.0
+ * conversion: for each block of 32 consecutive elements of a row, amax = max |w|;
  * if amax > 0 the shared exponent is floor(log2 amax) - 2, clamped to [-127, 127], and every
  * element w / 2^exponent is rounded to the nearest E2M1 magnitude (0, 0.5, 1, 1.5, 2, 3, 4, 6; ties
  * to the even code; above 6 saturates to 6) with its sign; a value that rounds to zero is +0 (code
