@@ -20,6 +20,13 @@
  * expert and shared MLPs, the weighted sum, the residual and layer_scalar) runs in fp64. bf16
  * inputs are widened exactly.
  *
+ * Pins. Every function declared here is checked against facts that do not come from the oracle
+ * (closed forms, library routines, the sparse == dense-masked identity, an independent float64
+ * brute force, the OCP MX rules): tests/test_oracle_pins.py, test_oracle_int8.py and
+ * test_oracle_fp4.py; tests/test_oracle_mutants.py checks that those pins fail on plausible
+ * mistakes planted in copies of moe_oracle.c. Agreement with the published checkpoint's own
+ * activations is parity unpinned: the pages print none and no checkpoint is at hand.
+ *
  * Dimensions are arguments, so the same code runs the real shapes and tiny brute-force shapes.
  * All arrays are dense row-major host memory. Tokens are independent and each token is computed
  * serially, so results do not depend on the number of threads.
