@@ -49,6 +49,17 @@ extern "C" {
 #define MOE_FFN_ECUDA (-5)    /* a CUDA runtime or driver call failed */
 #define MOE_FFN_EDEVICE (-6)  /* a kernel gave up a bounded wait or found a bad index and set the status word */
 
+/* Bits of the device status word (moe_ffn_device_status): which bounded wait gave up, or which
+ * check rejected an index. Several can be set at once. */
+#define MOE_FFN_STATUS_WAIT_FULL 0x1u       /* the MMA issuer gave up waiting for a filled stage */
+#define MOE_FFN_STATUS_WAIT_EMPTY 0x2u      /* a producer gave up waiting for a free stage */
+#define MOE_FFN_STATUS_WAIT_ACC_FULL 0x4u   /* an epilogue gave up waiting for an accumulator */
+#define MOE_FFN_STATUS_WAIT_ACC_EMPTY 0x8u  /* the MMA issuer gave up waiting for a drained accumulator */
+#define MOE_FFN_STATUS_BAD_INDEX 0x10u      /* an index read from the workspace was out of range */
+#define MOE_FFN_STATUS_BAD_SCHEDULE 0x20u   /* a tile list larger than its buffer */
+#define MOE_FFN_STATUS_DRAIN 0x40u          /* an exit drain gave up waiting for work in flight */
+#define MOE_FFN_STATUS_WAIT_ITEM 0x80u      /* a GEMM role gave up waiting for its next work item */
+
 /* Modes. */
 #define MOE_FFN_MOE_ONLY 0    /* router + experts only: out = sum of the 8 weighted expert outputs */
 #define MOE_FFN_FULL_LAYER 1  /* the whole dual-path feed-forward layer with norms, residual, layer_scalar */
@@ -173,7 +184,8 @@ int moe_ffn_workspace_view(const moe_ffn_ctx* ctx, moe_ffn_views* views);
 
 /* Synchronises `stream`, reads the device status word and clears it. Returns MOE_FFN_EDEVICE if a
  * kernel gave up a bounded wait or rejected an index since the last call, MOE_FFN_ECUDA if the
- * stream reported a CUDA error, else MOE_FFN_OK. *word (if not NULL) receives the raw status bits. */
+ * stream reported a CUDA error, else MOE_FFN_OK. *word (if not NULL) receives the raw status bits
+ * (MOE_FFN_STATUS_*). */
 int moe_ffn_device_status(moe_ffn_ctx* ctx, void* stream, uint32_t* word);
 
 /* Profiling hook: from now on every forward records `start` (a cudaEvent_t as void*) on its stream
@@ -233,11 +245,11 @@ int moe_ffn_quantize_mxfp4(const void* w, long long rows, int cols, uint8_t* cod
 /* Self-test of the bounded device waits behind MOE_FFN_EDEVICE (failure detection); the pages have
  * no counterpart. Queues on `stream` one kernel of one CTA that waits on an mbarrier nothing
  * arrives on, through the same helpers the forward's kernels wait with:
- *   wait 1, bounded: gives up after the 2 s limit, ORs 0x1 (a wait for a filled stage gave up)
- *           into *status_word and raises the CTA's abort flag;
- *   wait 2, bounded: leaves at once through the abort flag and sets nothing (its bit, 0x2, stays
- *           clear);
- *   wait 3, exit drain with a 1 ms limit: gives up and ORs 0x40.
+ *   wait 1, bounded: gives up after the 2 s limit, ORs MOE_FFN_STATUS_WAIT_FULL into
+ *           *status_word and raises the CTA's abort flag;
+ *   wait 2, bounded: leaves at once through the abort flag and sets nothing (its bit,
+ *           MOE_FFN_STATUS_WAIT_EMPTY, stays clear);
+ *   wait 3, exit drain with a 1 ms limit: gives up and ORs MOE_FFN_STATUS_DRAIN.
  * Nothing faults, traps or hangs; the kernel ends after about 2 s and the context stays usable.
  *   status_word  device pointer to one uint32 the caller has zeroed;
  *   record       device pointer to 6 uint64: record[2i] = nanoseconds wait i+1 took,

@@ -146,3 +146,17 @@ def test_plain_c_caller_links_the_library(lib, tmp_path):
         # No usable sm_103 device here: init reports a CUDA or architecture error and leaves NULL.
         rc, is_null = map(int, got["init"].split())
         assert rc in (B.MOE_FFN_ECUDA, B.MOE_FFN_EARCH) and is_null == 1
+
+
+def test_status_bits_match_the_kernels():
+    # The header's MOE_FFN_STATUS_* macros name the bits the kernels set (the kStatus* enum of the
+    # PTX layer), one to one and with the same values.
+    hdr = open(HEADER).read()
+    macros = {m.group(1): int(m.group(2), 16) for m in
+              re.finditer(r"#define MOE_FFN_STATUS_([A-Z_]+) (0x[0-9a-f]+)u", hdr)}
+    ptx = open(os.path.join(ROOT, "mixture_experts_ffn_router_gb300", "csrc", "ptx.cuh")).read()
+    enum = {m.group(1): 1 << int(m.group(2)) for m in re.finditer(r"kStatus(\w+) = 1u << (\d+)", ptx)}
+    snake = {re.sub(r"(?<!^)(?=[A-Z])", "_", k).upper(): v for k, v in enum.items()}
+    assert macros and macros == snake
+    # The status word of a forward holds nothing else.
+    assert sum(macros.values()) == 0xff
