@@ -21,6 +21,18 @@ MOE_FFN_EDEVICE = -6
 MOE_FFN_MOE_ONLY = 0
 MOE_FFN_FULL_LAYER = 1
 HIDDEN, N_EXPERTS, TOP_K, MOE_INTER, DENSE_INTER = 2816, 128, 8, 704, 2112
+# Bits of the device status word (MOE_FFN_STATUS_* in include/moe_ffn.h).
+STATUS_BITS = {"WAIT_FULL": 0x1, "WAIT_EMPTY": 0x2, "WAIT_ACC_FULL": 0x4, "WAIT_ACC_EMPTY": 0x8,
+               "BAD_INDEX": 0x10, "BAD_SCHEDULE": 0x20, "DRAIN": 0x40, "WAIT_ITEM": 0x80}
+
+
+def decode_status(word: int) -> list:
+    """Names of the bits set in a device status word, lowest first; unknown bits as hex."""
+    names = [n for n, b in sorted(STATUS_BITS.items(), key=lambda kv: kv[1]) if word & b]
+    rest = word & ~sum(STATUS_BITS.values())
+    return names + (["0x%x" % rest] if rest else [])
+
+
 KERNEL_NAMES = ("router_prep", "router_logits", "route_topk", "route_scatter", "gate_up_gemm", "down_gemm", "combine")
 
 _vp = ctypes.c_void_p

@@ -158,5 +158,8 @@ def test_status_bits_match_the_kernels():
     enum = {m.group(1): 1 << int(m.group(2)) for m in re.finditer(r"kStatus(\w+) = 1u << (\d+)", ptx)}
     snake = {re.sub(r"(?<!^)(?=[A-Z])", "_", k).upper(): v for k, v in enum.items()}
     assert macros and macros == snake
+    assert macros == B.STATUS_BITS
+    assert B.decode_status(0x41) == ["WAIT_FULL", "DRAIN"] and B.decode_status(0) == []
+    assert B.decode_status(0x102) == ["WAIT_EMPTY", "0x100"]
     # The status word of a forward holds nothing else.
     assert sum(macros.values()) == 0xff

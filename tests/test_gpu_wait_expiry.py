@@ -10,7 +10,7 @@ from tests import gpu_util as G
 
 pytestmark = pytest.mark.gpu
 
-WAIT_FULL, WAIT_EMPTY, DRAIN = 0x1, 0x2, 0x40
+WAIT_FULL, WAIT_EMPTY, DRAIN = (B.STATUS_BITS[k] for k in ("WAIT_FULL", "WAIT_EMPTY", "DRAIN"))
 
 
 def test_bounded_waits_give_up_and_report():
@@ -23,7 +23,7 @@ def test_bounded_waits_give_up_and_report():
     r = rec.cpu().tolist()
     # wait 1 gave up at the 2 s limit; wait 2 left through the abort flag without its own bit;
     # wait 3 (the exit drain, 1 ms limit) gave up too. None saw its phase complete.
-    assert word & WAIT_FULL and word & DRAIN and not word & WAIT_EMPTY, hex(word)
+    assert word & WAIT_FULL and word & DRAIN and not word & WAIT_EMPTY, B.decode_status(word)
     assert r[1] == 0 and r[3] == 0 and r[5] == 0, r
     assert 2.0e9 <= r[0] < 3.0e9, r
     assert r[2] < 1.0e8, r
