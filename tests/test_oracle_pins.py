@@ -281,3 +281,30 @@ def test_route_only_matches_forward():
         b = oracle.forward(d, x, w, want=want, route_only=True)
         for k in want:
             np.testing.assert_array_equal(a[k], b[k])
+
+
+# ---------------------------------------------------------------- degenerate cases
+
+def test_empty_batch():
+    x, w = tiny.case(tiny.SMALL, 0, 60, full_layer=True)
+    o = oracle.forward(tiny.dims_of(tiny.SMALL, full_layer=True), x, w, want=("out", "topk_idx", "topk_w"))
+    assert o["out"].shape == (0, tiny.SMALL["hidden"]) and o["topk_idx"].shape == (0, tiny.SMALL["top_k"])
+
+
+def test_top_one_routing_is_one_scaled_expert():
+    # With K = 1 the renormalised weight is exactly 1, so each token's expert branch is
+    # per_expert_scale[e] times one plain expert MLP (torch fp64 matmuls, library tanh GELU).
+    shape = dict(tiny.SMALL, top_k=1)
+    x, w = tiny.case(shape, 20, 61, full_layer=False, weight_std=0.3)
+    o = oracle.forward(tiny.dims_of(shape, full_layer=False), x, w, want=("out", "topk_idx", "topk_w", "topk_w_renorm"))
+    assert (o["topk_w_renorm"] == 1.0).all()
+    E, H, I = shape["n_experts"], shape["hidden"], shape["moe_inter"]
+    xt = torch.tensor(brute.bf16_to_f64(x).reshape(-1, H))
+    gu = torch.tensor(brute.bf16_to_f64(w["gate_up"]).reshape(E, 2 * I, H))
+    dn = torch.tensor(brute.bf16_to_f64(w["down"]).reshape(E, H, I))
+    for t in range(xt.shape[0]):
+        e = int(o["topk_idx"][t, 0])
+        g = gu[e] @ xt[t]
+        h = torch.nn.functional.gelu(g[:I], approximate="tanh") * g[I:]
+        ref = float(w["per_expert_scale"][e]) * (dn[e] @ h)
+        np.testing.assert_allclose(o["out"][t], ref.numpy(), rtol=0, atol=1e-11 * max(1.0, ref.abs().max().item()))
