@@ -54,3 +54,14 @@ def test_prefill_roofline_is_the_tensor_rate():
 def test_job_throughput_counts_every_rank():
     assert bench.job_throughput(64, 10, 1, 0.5) == pytest.approx(1280.0)
     assert bench.job_throughput(64, 10, 4, 0.5) == pytest.approx(5120.0)
+
+
+def test_default_run_follows_the_contract():
+    # No flags: one GPU, at least three warm-up steps, the decode workload the metric is quoted on,
+    # and the same arm the driver compares against the reference.
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1
+    assert a.impl == "ours" and a.workload == "decode64"
+    wl = bench.workload_of(a)
+    assert wl["T"] == 64 and wl["full"] and not wl["skew"]
+    assert bench.workload_of(bench.parse_args(["--workload", "prefill4096"]))["skew"]
