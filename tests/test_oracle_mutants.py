@@ -49,6 +49,9 @@ MUTANTS = [
     ("topk_takes_smallest", "logits[e] > logits[best]) best = e;", "logits[e] < logits[best]) best = e;"),
     ("gap_from_the_largest", "logits[order[K - 1]] - logits[order[K]]", "logits[order[0]] - logits[order[K]]"),
     ("no_renormalisation", "wren[j] = probs[idx[j]] / s;", "wren[j] = probs[idx[j]];"),
+    ("renormalised_over_all_experts", "for (int j = 0; j < K; ++j) s += probs[idx[j]];",
+     "for (int j = 0; j < E; ++j) s += probs[j];"),
+    ("gap_on_probabilities", "logits[order[K - 1]] - logits[order[K]]", "probs[order[K - 1]] - probs[order[K]]"),
     ("per_expert_scale_dropped", "wfin[j] = wren[j] * w->per_expert_scale[idx[j]];", "wfin[j] = wren[j];"),
     ("per_expert_scale_by_rank", "wfin[j] = wren[j] * w->per_expert_scale[idx[j]];", "wfin[j] = wren[j] * w->per_expert_scale[j];"),
     # expert MLP
@@ -57,6 +60,8 @@ MUTANTS = [
     ("expert_gate_up_stride", "const size_t g0 = (size_t)e * 2 * I;", "const size_t g0 = (size_t)e * I;"),
     ("expert_down_stride", "const size_t d0 = (size_t)e * H;", "const size_t d0 = (size_t)e * I;"),
     ("experts_read_raw_x", "expert_mlp(d, w, idx[k], n2, hv, y);", "expert_mlp(d, w, idx[k], xd, hv, y);"),
+    ("experts_only_input_normed", "for (int h = 0; h < H; ++h) n2[h] = xd[h];",
+     "moe_oracle_rmsnorm(xd, w->router_norm_w, H, (double)d->eps, n2);"),
     ("combine_without_per_expert_scale", "double c = (double)wfin[k] * y[h];", "double c = (double)wren[k] * y[h];"),
     ("masked_form_weights_unselected", "if (is_sel) we = (double)wfin[k];", "we = (double)wfin[k < K ? k : K - 1];"),
     # shared MLP
@@ -92,6 +97,8 @@ MUTANTS = [
     ("fp4_nibbles_swapped_on_decode", "const int code = (col & 1) ? (byte >> 4) : (byte & 15);",
      "const int code = (col & 1) ? (byte & 15) : (byte >> 4);"),
     ("fp4_grid_top_value_5", "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 5.0}"),
+    ("fp4_zero_keeps_its_sign", "return (best != 0 && v < 0) ? (best | 8) : best;",
+     "return (v < 0) ? (best | 8) : best;"),
     ("fp4_decode_drops_sign", "return ldexp((code & 8) ? -mag : mag, e);", "return ldexp(mag, e);"),
     # permutation
     ("permute_tokens_descending",
