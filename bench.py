@@ -7,9 +7,13 @@ GEMMs, combine with the post-norms) over one batch of synthetic tokens, through 
   python bench.py [--gpus N --steps K --warmup W] [--workload decode64|prefill4096|moe8|layer --T T]
   python bench.py --impl reference ...      (the oracle, timed on the host cores)
 
-Default workload: the full dual-path layer at decode batch T=64, uniform routing. Multi-GPU runs
-(torchrun, one rank per GPU) are weak scaling: each rank runs its own replica of the layer on its
-own 64 tokens; there is no data-path collective. Prints one JSON line (rank 0).
+Default workload: the full dual-path layer at decode batch T=64, uniform routing, which gives the
+line's `value`. The metric is quoted at T=64 and at T=4096, so the default run also measures, in
+the same process and under the same rules, the full layer at prefill T=4096 with Zipf(1.1)-skewed
+routing, and adds it to the same line as the `prefill4096` object (tokens/s, step time, layer and
+dominant-kernel rooflines, kernel breakdown, end-to-end figure, clocks). Multi-GPU runs (torchrun,
+one rank per GPU) are weak scaling: each rank runs its own replica of the layer on its own tokens;
+there is no data-path collective. Prints one JSON line (rank 0).
 """
 import argparse
 import json
@@ -87,6 +91,8 @@ def parse_args(argv=None):
     p.add_argument("--T", type=int, default=None, help="tokens per step for --workload layer")
     p.add_argument("--seed", type=int, default=1234)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="default workload only: skip the T=4096 prefill leg of the line")
     return p.parse_args(argv)
 
 
@@ -145,8 +151,10 @@ class ClockSampler:
     FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    CLOCK_PERIOD_MS = 50
+    SUSTAIN_S = 0.6
 
-    def __init__(self, uuid=None, period_ms=100):
+    def __init__(self, uuid=None, period_ms=CLOCK_PERIOD_MS):
         self.uuid = uuid
         self.period_ms = period_ms
         self.rows = []
@@ -180,12 +188,26 @@ class ClockSampler:
                 self.thread.join(timeout=5)
         return self
 
-    def summary(self, t0, t1):
-        rows = [r for (t, r) in self.rows if len(r) >= 10 and (self.uuid is None or self.uuid in r[1])]
-        timed = [r for (t, r) in self.rows if t0 <= t <= t1 and len(r) >= 10 and (self.uuid is None or self.uuid in r[1])]
-        use = timed or rows
+    def rows_between(self, t0, t1):
+        return [r for (t, r) in self.rows
+                if t0 <= t <= t1 and len(r) >= 10 and (self.uuid is None or self.uuid in r[1])]
+
+    def summary(self, t0, t1, s0=None, s1=None):
+        """Clocks during the timed region [t0, t1]. If no sample fell inside it (a region shorter
+        than the sampling period), the samples of the sustained run of the same step [s0, s1] that
+        followed it, and `window` says which."""
+        timed = self.rows_between(t0, t1)
+        if timed:
+            use, window = timed, "timed region"
+        elif s0 is not None:
+            use = self.rows_between(s0, s1)
+            window = ("no sample inside the %.1f ms timed region (sampling period %d ms); these are the samples "
+                      "of the same step run for %.1f s right after it" % ((t1 - t0) * 1e3, self.period_ms, s1 - s0))
+        else:
+            use, window = [], "no sample inside the timed region"
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "in_timed_region": False,
+                    "window": window}
 
         def num(x):
             try:
@@ -202,7 +224,7 @@ class ClockSampler:
                     reasons.add(n)
         pw = [num(r[4]) for r in use if num(r[4]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(timed),
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(timed), "window": window,
                 "power_w_max": max(pw) if pw else None}
 
 
@@ -283,7 +305,7 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": steps,
         "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (router f32)", "data": "synthetic",
-        "config": {"workload": wl["desc"], "T": T},
+        "config": config_of(wl, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -293,31 +315,31 @@ def run_reference(args, wl):
 
 # ------------------------------------------------------------------ the GPU arm
 
-def run_ours(args, wl):
+def config_of(wl, world):
+    """The `config` object of a JSON line, the same for the GPU arm and the reference arm."""
+    return {"workload": wl["desc"], "T": wl["T"], "tokens_per_gpu": wl["T"], "hidden": H, "experts": E, "top_k": K,
+            "moe_inter": I, "dense_inter": D if wl["full"] else 0,
+            "expert_weights": ("int8, per-row fp32 scale" if wl.get("int8") else
+                               "MXFP4 (E2M1, E8M0 scale per 32 weights)" if wl.get("fp4") else "bf16"),
+            "layers": wl.get("layers", 1),
+            "l2": "inputs larger than L2: every step reads the routed experts' weights (11.9 MB per expert hit, "
+                  "1.52 GB for all 128) and the shared MLP's 35.7 MB, against a 126 MB L2",
+            "parallelism": "replicas (dp%d, no collective)" % world}
+
+
+def measure(args, wl, weights, x, dev, world, rank, with_cpu, clocks, label):
+    """Times one workload: untimed breakdown pass, exactly args.steps timed steps (CUDA events on the
+    launching stream, barrier + synchronize on both sides), the end-to-end leg with host buffers,
+    and the clocks seen while that workload ran. Returns the numbers of one JSON line."""
     import numpy as np
     import torch
     from mixture_experts_ffn_router_gb300 import binding as B
     from mixture_experts_ffn_router_gb300 import synth
 
-    rank, world = dist_init("nccl")
-    _, _, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     T = wl["T"]
-    mode = B.MOE_FFN_FULL_LAYER if wl["full"] else B.MOE_FFN_MOE_ONLY
-
     L = wl.get("layers", 1)
-    # One context per layer, all sharing the first one's workspace (their forwards never overlap).
-    weights = [synth.make_weights(seed=args.seed, layer=l, device=dev, full_layer=wl["full"], skew=wl["skew"])
-               for l in range(L)]
-    if wl.get("int8") or wl.get("fp4"):
-        # int8 or MXFP4 experts, made on the device; the bf16 experts are then dropped.
-        q = B.quantize_experts_int8 if wl.get("int8") else B.quantize_experts_mxfp4
-        weights = [q(w) for w in weights]
-        torch.cuda.synchronize()
-        for w in weights:
-            del w["gate_up"], w["down"]
-    x = synth.make_x(T, seed=args.seed, device=dev)
+    mode = B.MOE_FFN_FULL_LAYER if wl["full"] else B.MOE_FFN_MOE_ONLY
+    local = dev.index
     bufs = [torch.empty_like(x), torch.empty_like(x)]
     ctxs = [B.MoeFFN(mode, T, device=local)]
     for _ in range(1, L):
@@ -344,7 +366,7 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     rc, word = m.status()
     if rc != B.MOE_FFN_OK:
-        raise RuntimeError("device status 0x%x after warm-up" % word)
+        raise RuntimeError("%s: device status 0x%x after warm-up" % (label, word))
     hits = []
 
     def count_hits(l):
@@ -395,13 +417,7 @@ def run_ours(args, wl):
     timed_dom = [i for i in range(args.steps) if i % DOM_EVERY == 0]
     ev = event_pairs(len(timed_dom))
     torch.cuda.synchronize()
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        uuid = None
-    clocks = ClockSampler(uuid=uuid).start()
-    time.sleep(0.3)
+    time.sleep(0.15)  # let the clock sampler see the GPU idle-to-busy edge on its own samples
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world, dev)
     torch.cuda.synchronize()
@@ -419,11 +435,20 @@ def run_ours(args, wl):
     wall1 = time.time()
     barrier(world, dev)
     B.moe_ffn_set_kernel_events(mk.ctx, dom_k, None, None)
-    time.sleep(0.25)
-    clocks.stop()
     rc, word = m.status()
     if rc != B.MOE_FFN_OK:
-        raise RuntimeError("device status 0x%x after the timed steps" % word)
+        raise RuntimeError("%s: device status 0x%x after the timed steps" % (label, word))
+    # The sampler's period is CLOCK_PERIOD_MS; a timed region shorter than that holds no sample of
+    # its own. The same step then runs, untimed, for SUSTAIN_S right after the timed region, and
+    # the clocks of that window are reported instead, marked as such.
+    sus0 = sus1 = None
+    if clocks is not None and (wall1 - wall0) * 1e3 < 4 * ClockSampler.CLOCK_PERIOD_MS:
+        sus0 = time.time()
+        while time.time() - sus0 < ClockSampler.SUSTAIN_S:
+            for _ in range(8):
+                step()
+            torch.cuda.synchronize()
+        sus1 = time.time()
 
     ms = t_start.elapsed_time(t_stop)
     ms_max = max_over_ranks(ms, world, dev)
@@ -456,8 +481,9 @@ def run_ours(args, wl):
     else:
         roof = {"bound": "tensor", "achieved": kf / dur_s / 1e12, "peak": tc_burst, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_record(dom, args.workload if args.workload != "layer" else "layer_T%d" % T)
+    roof["traffic"] = traffic_record(dom, label if label != "layer" else "layer_T%d" % T)
     roof["kernel"] = dom
+    roof["kernel_us"] = dom_us
     roof["algorithmic_bytes"] = kb
     roof["algorithmic_flops"] = kf
     roof["peak_source"] = peak_src
@@ -480,27 +506,27 @@ def run_ours(args, wl):
     x_dev = [torch.empty_like(x), torch.empty_like(x)]
     o_dev = [torch.empty_like(x), torch.empty_like(x)]
     h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "fwd", "out")}
+    eev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "fwd", "out")}
 
     def e2e_steps(n):
         for i in range(n):
             j = i % 2
             if i >= 2:
-                h2d.wait_event(ev["fwd"][j])      # step i-2 has finished reading x_dev[j]
+                h2d.wait_event(eev["fwd"][j])      # step i-2 has finished reading x_dev[j]
             with torch.cuda.stream(h2d):
                 x_dev[j].copy_(x_host, non_blocking=True)
-            ev["in"][j].record(h2d)
-            stream.wait_event(ev["in"][j])
+            eev["in"][j].record(h2d)
+            stream.wait_event(eev["in"][j])
             if i >= 2:
-                stream.wait_event(ev["out"][j])   # step i-2's output has left o_dev[j]
+                stream.wait_event(eev["out"][j])   # step i-2's output has left o_dev[j]
             step(x_in=x_dev[j], x_out=o_dev[j])
-            ev["fwd"][j].record(stream)
-            d2h.wait_event(ev["fwd"][j])
+            eev["fwd"][j].record(stream)
+            d2h.wait_event(eev["fwd"][j])
             with torch.cuda.stream(d2h):
                 out_host.copy_(o_dev[j], non_blocking=True)
-            ev["out"][j].record(d2h)
+            eev["out"][j].record(d2h)
         for j in range(2):
-            stream.wait_event(ev["out"][j])
+            stream.wait_event(eev["out"][j])
 
     e2e_steps(3)
     torch.cuda.synchronize()
@@ -519,33 +545,83 @@ def run_ours(args, wl):
     torch.testing.assert_close(out_host, o_dev[(e_steps - 1) % 2].cpu(), rtol=0, atol=0)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if with_cpu:
         n = min(T, 64)
         tps, cores, secs, passes = oracle_tokens_per_s(wl, synth.host_arrays(weights[0]), synth.bf16_bits(x), n)
         cpu = {"value": tps / L, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "first %d tokens of the step's batch through layer 0, %d passes, %.1f s of oracle time%s"
                          % (n, passes, secs, "; the stack rate is that layer rate / %d" % L if L > 1 else "")}
 
-    clk = clocks.summary(wall0, wall1)
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl["desc"], "T": T, "tokens_per_gpu": T, "hidden": H, "experts": E, "top_k": K,
-                       "moe_inter": I, "dense_inter": D if wl["full"] else 0,
-                       "expert_weights": ("int8, per-row fp32 scale" if wl.get("int8") else
-                                          "MXFP4 (E2M1, E8M0 scale per 32 weights)" if wl.get("fp4") else "bf16"),
-                       "layers": L,
-                       "l2": "inputs larger than L2 (%.2f GB of weights read per step)" % (layer_bytes * L / 1e9),
-                       "parallelism": "replicas (dp%d, no collective)" % world},
-            "roofline": roof, "layer_roofline": layer, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": nk * L * args.steps, "clocks": clk,
-            "kernels_us": kernel_us, "kernels_us_note": "untimed breakdown pass, %d steps, events around every kernel" % n_b,
-        }
-        print(json.dumps(line), flush=True)
+    clk = clocks.summary(wall0, wall1, sus0, sus1) if clocks is not None else None
     for c in ctxs:
         c.close()
+    return {"value": value, "ms_per_step": ms_max / args.steps, "roofline": roof, "layer_roofline": layer,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * L * args.steps, "clocks": clk,
+            "kernels_us": kernel_us,
+            "kernels_us_note": "untimed breakdown pass, %d steps, events around every kernel" % n_b}
+
+
+def run_ours(args, wl):
+    import torch
+    from mixture_experts_ffn_router_gb300 import synth
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T = wl["T"]
+    L = wl.get("layers", 1)
+    weights = [synth.make_weights(seed=args.seed, layer=l, device=dev, full_layer=wl["full"], skew=wl["skew"])
+               for l in range(L)]
+    if wl.get("int8") or wl.get("fp4"):
+        from mixture_experts_ffn_router_gb300 import binding as B
+        # int8 or MXFP4 experts, made on the device; the bf16 experts are then dropped.
+        q = B.quantize_experts_int8 if wl.get("int8") else B.quantize_experts_mxfp4
+        weights = [q(w) for w in weights]
+        torch.cuda.synchronize()
+        for w in weights:
+            del w["gate_up"], w["down"]
+    x = synth.make_x(T, seed=args.seed, device=dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid=uuid).start()
+    time.sleep(0.3)
+    res = measure(args, wl, weights, x, dev, world, rank, rank == 0 and world == 1 and not args.no_cpu_baseline,
+                  clocks, args.workload)
+
+    # The metric is quoted at decode T=64 and at prefill T=4096: the default run measures both in
+    # this process. The prefill leg runs the same layer's weights with the skewed router rows
+    # (Zipf(1.1) row scales, the same draw the prefill4096 workload makes) on 4096 tokens.
+    prefill = None
+    if args.workload == "decode64" and not args.no_prefill:
+        wl_p = workload_of(argparse.Namespace(workload="prefill4096", T=None))
+        w_p = dict(weights[0])
+        w_p["router_w"] = synth.make_router_w(seed=args.seed, layer=0, device=dev, skew=True)
+        x_p = synth.make_x(wl_p["T"], seed=args.seed, device=dev)
+        prefill = measure(args, wl_p, [w_p], x_p, dev, world, rank, False, clocks, "prefill4096")
+        prefill = {"metric": METRIC, "unit": UNIT, "steps": args.steps, "warmup": max(args.warmup, 3),
+                   "config": config_of(wl_p, world), **prefill}
+        del prefill["cpu_baseline"]
+    time.sleep(0.25)
+    clocks.stop()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl, world),
+            "roofline": res["roofline"], "layer_roofline": res["layer_roofline"], "cpu_baseline": res["cpu_baseline"],
+            "e2e": res["e2e"], "gpu_launches": res["gpu_launches"] + (prefill["gpu_launches"] if prefill else 0),
+            "gpu_launches_note": "both timed regions (decode and prefill legs)" if prefill else "the timed region",
+            "clocks": res["clocks"], "kernels_us": res["kernels_us"], "kernels_us_note": res["kernels_us_note"],
+        }
+        if prefill is not None:
+            line["prefill4096"] = prefill
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -214,10 +214,14 @@ int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
  * It allocates nothing: its scratch is one array of about 2.6 MB in device memory that the library
  * reserves on each GPU it runs on, held until the process exits. Every call shares that array, so
  * calls whose GPU work overlaps in time (other streams, other host threads) race and corrupt each
- * other's results; every byte a call reads there is written earlier in the same call, so nothing
- * needs clearing. It runs on the calling thread's current CUDA device. The first call on a device
- * looks up the array's device address and builds a TMA descriptor over it; make that first call
- * before any stream capture. All pointers must be 16-byte aligned (MOE_FFN_EALIGN). */
+ * other's results. The array keeps the last call's contents: each call clears its status word
+ * first (an asynchronous memset on `stream`), and every other byte it reads there it has written
+ * itself. Calls queued back to back on one stream are ordered and do not race. It runs on the
+ * calling thread's current CUDA device. The first call on a device looks up the array's device
+ * address and builds a TMA descriptor over it; make that first call before any stream capture.
+ * All pointers must be 16-byte aligned (MOE_FFN_EALIGN).
+ * Failure: if one of the router's bounded device waits gives up (MOE_FFN_STATUS_* above), that
+ * call writes NaN to all T x 128 logits; the return value only covers errors found while queueing. */
 int moe_ffn_router_logits_noalloc(const void* x, int T, const float* router_w, const float* router_norm_w,
                                   float router_scale, float eps, float* logits, void* stream);
 

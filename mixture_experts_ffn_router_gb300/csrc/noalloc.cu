@@ -10,9 +10,16 @@
 // The scratch: g_router_scratch below, kNoAllocScratchBytes (about 2.6 MB) of device memory on
 // every GPU the process uses with this library, held until the process exits. It holds the split
 // router matrix (3 x 128 x 2816 bf16), the partial logits of up to kNoAllocMaxTokens tokens and a
-// few control words. Every byte a call reads there is written earlier by the same call, so no
-// clearing is needed; but all calls share the one array, so two calls whose GPU work overlaps in
-// time (different streams, or different host threads) corrupt each other's results.
+// few control words. The array keeps what the last call left there. Each call first clears its
+// status word (an asynchronous memset on the caller's stream, which allocates nothing); every
+// other byte a call reads there is written earlier by the same call. All calls share the one
+// array, so two calls whose GPU work overlaps in time (different streams, or different host
+// threads) corrupt each other's results.
+//
+// Failure: the tensor-core router's waits are bounded; one that gives up sets the status word and
+// the kernel writes no partial sums. The finishing kernel reads the word and then writes NaN to
+// every logit of the call instead of logits made from stale partial sums, so a failed call can
+// never pass for a good one.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -51,12 +58,19 @@ std::mutex g_setup_mutex;
 
 // One warp per token: logits = partial sum * (1 / rms(x)) * router_scale, with the RMS taken as
 // in the top-k kernel (fp32, eps inside the square root).
+// If the status word is set (a bounded wait of the router gave up), every logit is NaN.
 __global__ void __launch_bounds__(256) finish_logits_kernel(const uint16_t* x, const float* part, int T,
-                                                            float eps, float scale, float* logits) {
+                                                            float eps, float scale, const unsigned int* status,
+                                                            float* logits) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   pdl_wait();
   if (t >= T) return;
+  if (*reinterpret_cast<const volatile unsigned int*>(status) != 0u) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) logits[static_cast<size_t>(t) * E + lane + 32 * j] = __int_as_float(0x7fc00000);
+    return;
+  }
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
   float ss = 0.0f;
 #pragma unroll
@@ -139,10 +153,13 @@ extern "C" int moe_ffn_router_logits_noalloc(const void* x, int T, const float* 
   p.router_scale = router_scale;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The status word starts every call at zero (the array keeps the last call's contents).
+  if (cudaMemsetAsync(b.status, 0, sizeof(unsigned int), s) != cudaSuccess) return MOE_FFN_ECUDA;
   if (launch_router_prep(p, b, s) != cudaSuccess) return MOE_FFN_ECUDA;
   if (launch_router_logits(dev->map_wsplit, p, b, s) != cudaSuccess) return MOE_FFN_ECUDA;
   if (launch_pdl(finish_logits_kernel, dim3((T + 7) / 8), dim3(256), 0, s, p.x,
-                 static_cast<const float*>(b.logits_part), T, eps, router_scale, logits) != cudaSuccess)
+                 static_cast<const float*>(b.logits_part), T, eps, router_scale,
+                 static_cast<const unsigned int*>(b.status), logits) != cudaSuccess)
     return MOE_FFN_ECUDA;
   return MOE_FFN_OK;
 }

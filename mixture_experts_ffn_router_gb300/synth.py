@@ -74,15 +74,22 @@ def skew_scales(seed: int = 1234, layer: int = 0, dims=GEMMA, s: float = ZIPF_S)
     return rank.pow(-s).to(torch.float32)
 
 
+def make_router_w(seed: int = 1234, layer: int = 0, device="cpu", skew: bool = False, dims=GEMMA) -> torch.Tensor:
+    """The router matrix [E, H] fp32 ~ N(0, 1), rows scaled by c_e for the skewed workload. The
+    same tensor make_weights draws, so a caller holding one layer's weights can switch it between
+    uniform and skewed routing without drawing the expert weights again."""
+    rw = _normal((dims["n_experts"], dims["hidden"]), 1.0, seed, layer, "router_w", "cpu", torch.float32)
+    if skew:
+        rw.mul_(skew_scales(seed, layer, dims)[:, None])
+    return rw.to(device)
+
+
 def make_weights(seed: int = 1234, layer: int = 0, device="cpu", full_layer: bool = True,
                  skew: bool = False, dims=GEMMA, layer_scalar: float = LAYER_SCALAR) -> dict:
     """One layer's weights as torch tensors on ``device`` (see the module docstring)."""
     H, E, I, D = dims["hidden"], dims["n_experts"], dims["moe_inter"], dims["dense_inter"]
     w = {}
-    rw = _normal((E, H), 1.0, seed, layer, "router_w", "cpu", torch.float32)
-    if skew:
-        rw.mul_(skew_scales(seed, layer, dims)[:, None])
-    w["router_w"] = rw.to(device)
+    w["router_w"] = make_router_w(seed, layer, device, skew, dims)
     w["router_norm_w"] = _normal((H,), 0.1, seed, layer, "router_norm_w", "cpu", torch.float32).to(device)
     g = _gen(seed, layer, "per_expert_scale")
     w["per_expert_scale"] = (torch.rand(E, generator=g, dtype=torch.float32) + 0.5).to(device)

@@ -65,3 +65,33 @@ def test_default_run_follows_the_contract():
     wl = bench.workload_of(a)
     assert wl["T"] == 64 and wl["full"] and not wl["skew"]
     assert bench.workload_of(bench.parse_args(["--workload", "prefill4096"]))["skew"]
+
+
+def test_reference_and_gpu_arms_print_the_same_config():
+    # The driver compares the two arms' lines; both build `config` from one function.
+    for name in ("decode64", "prefill4096", "moe8"):
+        wl = bench.workload_of(bench.parse_args(["--workload", name]))
+        assert bench.config_of(wl, 1) == bench.config_of(dict(wl), 1)
+        assert bench.config_of(wl, 1)["T"] == wl["T"]
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert src.count('"config": config_of(wl, world)') == 2
+
+
+def test_default_run_adds_the_prefill_leg():
+    # The metric is quoted at T=64 and at T=4096: the default run measures both.
+    a = bench.parse_args([])
+    assert not a.no_prefill
+    wl = bench.workload_of(bench.argparse.Namespace(workload="prefill4096", T=None))
+    assert wl["T"] == 4096 and wl["skew"] and wl["full"]
+
+
+def test_clock_summary_names_its_window():
+    c = bench.ClockSampler(uuid=None)
+    row = ["0", "GPU-x", "2070", "2070", "500", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    c.rows = [(10.0, row), (10.5, row), (11.2, row)]
+    inside = c.summary(9.9, 10.6)
+    assert inside["in_timed_region"] and inside["samples"] == 2 and inside["window"] == "timed region"
+    after = c.summary(10.6, 10.61, 11.0, 11.5)
+    assert not after["in_timed_region"] and after["samples"] == 1 and "right after" in after["window"]
+    none = c.summary(10.6, 10.61)
+    assert none["samples"] == 0 and not none["in_timed_region"]

@@ -42,7 +42,7 @@ def test_moe_only_small(T):
     _full_check(MOE, T, 100 + T, label="moe-only T=%d" % T)
 
 
-@pytest.mark.parametrize("T", [64, 1, 65, 200])
+@pytest.mark.parametrize("T", [64, 1, 16, 65, 200])
 def test_full_layer(T):
     _full_check(FULL, T, 200 + T, label="full T=%d" % T)
 
@@ -74,6 +74,13 @@ def test_full_layer_prefill_skewed_4096():
 @pytest.mark.parametrize("T", [256, 777, 1024, 1500])
 def test_full_layer_sweep_sizes(T):
     _sampled_check(FULL, T, 400 + T, False, 32, "full T=%d" % T)
+
+
+def test_full_layer_prefill_uniform_4096():
+    # The sweep's T=4096 point: uniform routing, so nearly every expert gets two token tiles of 256
+    # (the second one partly filled).
+    run, _ = _sampled_check(FULL, 4096, 450, False, 32, "full T=4096 uniform")
+    assert (run.counts > 0).sum() == 128
 
 
 @pytest.mark.slow
@@ -143,3 +150,46 @@ def test_error_paths():
     assert B.moe_ffn_workspace_bytes(cfg) == 0
     torch.cuda.synchronize()
     assert m.status() == (B.MOE_FFN_OK, 0)
+
+
+def test_all_zero_input_row():
+    # A token whose input row is all zero: RMS is sqrt(eps), every logit is exactly 0, so all 128
+    # experts tie and the tie rule picks experts 0..7 with equal renormalised weights (times
+    # per_expert_scale); its expert inputs, expert outputs and shared-MLP output are zero, so the
+    # post-norms give zero and the output row is (0 + 0) * layer_scalar = 0.
+    T, z = 64, 5
+    x, w = G.make_case(FULL, T, 1000)
+    x[z].zero_()
+    run, ref, _, _ = _full_check_inputs(FULL, x, w, "full T=64 with a zero row")
+    np.testing.assert_array_equal(run.topk_idx[z], np.arange(8))
+    np.testing.assert_array_equal(ref["topk_idx"][z], np.arange(8))
+    assert run.gap[z] == 0.0 and (run.logits[z] == 0.0).all()
+    pes = w["per_expert_scale"].cpu().numpy()[:8]
+    np.testing.assert_allclose(run.topk_w[z], pes / 8.0, rtol=1e-6)
+    assert (run.out_f64[z] == 0.0).all() and np.isfinite(run.out_f64).all()
+
+
+@pytest.mark.parametrize("scale", [1e3, 1e-3])
+def test_extreme_input_magnitudes(scale):
+    # x scaled by 1e3 or 1e-3 (about 1e-6 mean square, the size of eps). The router and the
+    # pre-norms see RMS-normalised rows, so the routing checks are unchanged; the output holds the
+    # residual term x * layer_scalar, whose bf16 rounding is relative (half an ulp is 2^-9 of the
+    # value), so the absolute bar grows by 2^-8 of the oracle's magnitude.
+    T = 64
+    x, w = G.make_case(FULL, T, 1100 + int(scale > 1))
+    x = (x.float() * scale).to(torch.bfloat16)
+    run, ref, frob, mx = _full_check_inputs(FULL, x, w, "full T=64, x * %g" % scale, rel_abs=2.0 ** -8)
+    assert np.isfinite(run.out_f64).all()
+
+
+def _full_check_inputs(mode, x, w, label, rel_abs=0.0):
+    run = G.Run(mode, x, w)
+    ref = G.oracle_forward(mode, synth.bf16_bits(x), G.host_weights(w))
+    same = G.check_routing(run, ref)
+    G.check_permutation(run)
+    got, want = run.out_f64[same], ref["out"][same]
+    frob, mx = G.errors(got, want)
+    assert frob <= G.FROB_TOL, "%s rel Frobenius %.3e" % (label, frob)
+    excess = np.abs(got - want) - (G.MAXABS_TOL + rel_abs * np.abs(want))
+    assert (excess <= 0).all(), "%s max abs %.3e beyond the bar" % (label, mx)
+    return run, ref, frob, mx
