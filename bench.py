@@ -379,7 +379,6 @@ def measure(args, wl, weights, x, dev, world, rank, with_cpu, clocks, label):
 
     # Breakdown pass (untimed): events around every kernel slot of each forward, to rank the
     # kernels (a slot a forward of this size leaves empty records its two events back to back).
-    nk = B.moe_ffn_kernels_per_forward(m.ctx, T)
     nslots = len(B.KERNEL_NAMES)
     n_b = max(1, min(50, args.steps))
 
@@ -401,8 +400,9 @@ def measure(args, wl, weights, x, dev, world, rank, with_cpu, clocks, label):
     torch.cuda.synchronize()
     for k in range(nslots):
         B.moe_ffn_set_kernel_events(mk.ctx, k, None, None)
-    # A forward with fewer kernels than slots leaves the fold slot (0) empty: not reported.
-    used = [k for k in range(nslots) if nk == nslots or k != 0]
+    # Slots a forward of this size leaves empty are not reported.
+    used = B.moe_ffn_kernel_slots(m.ctx, T)
+    nk = len(used)
     kernel_us = {B.KERNEL_NAMES[k]: float(np.mean([bd[i][k][0].elapsed_time(bd[i][k][1]) for i in range(n_b)]) * 1e3)
                  for k in used}
     gemms = {"gate_up_gemm": B.KERNEL_NAMES.index("gate_up_gemm"), "down_gemm": B.KERNEL_NAMES.index("down_gemm")}

@@ -59,6 +59,8 @@ extern "C" {
 #define MOE_FFN_STATUS_BAD_SCHEDULE 0x20u   /* a tile list larger than its buffer */
 #define MOE_FFN_STATUS_DRAIN 0x40u          /* an exit drain gave up waiting for work in flight */
 #define MOE_FFN_STATUS_WAIT_ITEM 0x80u      /* a GEMM role gave up waiting for its next work item */
+#define MOE_FFN_STATUS_WAIT_COPY 0x100u     /* a GEMM producer gave up waiting for the sorted copy of
+                                               its token rows (forwards above 1024 tokens) */
 
 /* Modes. */
 #define MOE_FFN_MOE_ONLY 0    /* router + experts only: out = sum of the 8 weighted expert outputs */
@@ -142,7 +144,10 @@ typedef struct moe_ffn_views {
   const float* w_sorted;      /* [S] the weight of each sorted slot */
   const int32_t* slot_pos;    /* [T, 8] sorted position of slot (t, k) */
   const uint16_t* n1;         /* [T, 2816] bf16 pre_feedforward_layernorm(x) (FULL_LAYER) */
-  const uint16_t* n2;         /* [T, 2816] bf16 expert input: pre_feedforward_layernorm_2(x), or x */
+  const uint16_t* n2;         /* [T, 2816] bf16 expert input: pre_feedforward_layernorm_2(x), or x
+                               (forwards of at most 1024 tokens or with converted experts; larger
+                               ones write it in sorted-slot order into the y buffer instead, which the
+                               down GEMM then overwrites) */
   const uint16_t* h;          /* [S, 704] bf16 gelu_tanh(gate) * up per sorted slot */
   const uint16_t* h_dense;    /* [T, 2112] bf16 shared-MLP activation (FULL_LAYER) */
   const uint16_t* y;          /* [S, 2816] bf16 weighted expert output per sorted slot */
@@ -189,16 +194,21 @@ int moe_ffn_workspace_view(const moe_ffn_ctx* ctx, moe_ffn_views* views);
 int moe_ffn_device_status(moe_ffn_ctx* ctx, void* stream, uint32_t* word);
 
 /* Profiling hook: from now on every forward records `start` (a cudaEvent_t as void*) on its stream
- * right before the launch of kernel `kernel` and `stop` right after it. NULL events turn the hook
- * off. kernel: 0 router matrix split, 1 router logits, 2 top-k and pre-norms, 3 permutation,
- * 4 gate_up grouped GEMM, 5 down grouped GEMM, 6 combine and post-norms. Forwards of at most 64
- * tokens launch nothing at slot 0 (their router sums run on CUDA cores in slot 1), so its two
- * events are recorded back to back. */
+ * right before the launch of kernel slot `kernel` and `stop` right after it. NULL events turn the
+ * hook off. Slots (0..6): 0 router matrix split, 1 router logits, 2 top-k and pre-norms,
+ * 3 permutation (counting-sort scatter), 4 gate_up grouped GEMM, 5 down grouped GEMM, 6 combine and
+ * post-norms. Forwards of at most 64 tokens launch nothing at slot 0 (their router sums run on CUDA
+ * cores in slot 1), so its two events are recorded back to back (moe_ffn_kernel_slots). */
 int moe_ffn_set_kernel_events(moe_ffn_ctx* ctx, int kernel, void* start, void* stop);
 
 /* Number of kernels one forward of T tokens launches on the device (0 for T = 0; 6 for T <= 64,
  * else 7). */
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
+
+/* The kernel slots (see moe_ffn_set_kernel_events) one forward of T tokens launches, in launch
+ * order, written to slots[0..n-1]; returns n (or MOE_FFN_EINVAL: NULL ctx or slots, T < 0, or
+ * n_slots below 7). Host only. */
+int moe_ffn_kernel_slots(const moe_ffn_ctx* ctx, int T, int* slots, int n_slots);
 
 /* The block's fp32 router logits, [T, 128], for callers that cannot allocate device memory (code
  * running under a memory pool or allocator it does not own, a plugin handed only a stream and its

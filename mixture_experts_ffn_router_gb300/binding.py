@@ -23,7 +23,8 @@ MOE_FFN_FULL_LAYER = 1
 HIDDEN, N_EXPERTS, TOP_K, MOE_INTER, DENSE_INTER = 2816, 128, 8, 704, 2112
 # Bits of the device status word (MOE_FFN_STATUS_* in include/moe_ffn.h).
 STATUS_BITS = {"WAIT_FULL": 0x1, "WAIT_EMPTY": 0x2, "WAIT_ACC_FULL": 0x4, "WAIT_ACC_EMPTY": 0x8,
-               "BAD_INDEX": 0x10, "BAD_SCHEDULE": 0x20, "DRAIN": 0x40, "WAIT_ITEM": 0x80}
+               "BAD_INDEX": 0x10, "BAD_SCHEDULE": 0x20, "DRAIN": 0x40, "WAIT_ITEM": 0x80,
+               "WAIT_COPY": 0x100}
 
 
 def decode_status(word: int) -> list:
@@ -91,6 +92,8 @@ def lib():
         L.moe_ffn_set_kernel_events.argtypes = [_vp, ctypes.c_int, _vp, _vp]
         L.moe_ffn_kernels_per_forward.restype = ctypes.c_int
         L.moe_ffn_kernels_per_forward.argtypes = [_vp, ctypes.c_int]
+        L.moe_ffn_kernel_slots.restype = ctypes.c_int
+        L.moe_ffn_kernel_slots.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         L.moe_ffn_router_logits_noalloc.restype = ctypes.c_int
         L.moe_ffn_router_logits_noalloc.argtypes = [_vp, ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                                      _vp, _vp]
@@ -165,6 +168,15 @@ def moe_ffn_set_kernel_events(ctx: int, kernel: int, start: int, stop: int) -> i
 
 def moe_ffn_kernels_per_forward(ctx: int, T: int) -> int:
     return lib().moe_ffn_kernels_per_forward(_vp(ctx), int(T))
+
+
+def moe_ffn_kernel_slots(ctx: int, T: int) -> list:
+    """The kernel slots a forward of T tokens launches, in launch order."""
+    buf = (ctypes.c_int * len(KERNEL_NAMES))()
+    n = lib().moe_ffn_kernel_slots(_vp(ctx), int(T), buf, len(KERNEL_NAMES))
+    if n < 0:
+        raise MoeFFNError("moe_ffn_kernel_slots", n)
+    return list(buf[:n])
 
 
 def moe_ffn_router_logits_noalloc(x: int, T: int, router_w: int, router_norm_w: int, router_scale: float,

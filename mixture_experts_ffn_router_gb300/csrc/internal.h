@@ -33,7 +33,8 @@ struct Buffers {
   int32_t* offsets;     // [129]
   int32_t* n_exp_tiles; // [1]
   int32_t* done_ctr;    // [1]
-  int32_t* sched;       // [2] work-item counters of the gate_up and down GEMMs (zeroed by top-k)
+  int32_t* sched;       // [3] work-item counters of the gate_up and down GEMMs, and the count of
+                        // warps that finished the sorted copy of n2 (all zeroed by top-k)
   int4* exp_tiles;      // [max_tiles] (expert, first sorted row, rows, 0), grouped by expert
   int32_t* tile_off;    // [129] index of each expert's first token tile in exp_tiles
   int32_t* perm;        // [S]
@@ -44,6 +45,7 @@ struct Buffers {
   uint16_t* h;          // [S, 704]
   uint16_t* h_dense;    // [Tm, 2112]
   uint16_t* y;          // [S, 2816] bf16
+  uint16_t* n2s;        // [S, 2816] bf16: n2 rows in sorted-slot order (T > kPermRowsT), aliases y
   float* d;             // [Tm, 2816]
   unsigned int* status; // [1]
   uint16_t* wsplit;     // [3, 128, 2816] bf16: W_r * (1 + router_norm_w) as hi + mid + lo
@@ -64,6 +66,7 @@ struct RouteParams {
   int tpw;              // tokens per warp in the top-k kernel
   int bn;               // token-tile width of the grouped GEMMs
   int full_layer;
+  int write_n2;         // the top-k kernel writes n2 (token order); else the gate_up GEMM writes n2s
   float eps;
   float router_scale;
 };
@@ -129,7 +132,13 @@ inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Kernel slots of one forward (events, breakdown): 0 router prep, 1 router logits, 2 top-k,
+// 3 scatter, 4 gate_up, 5 down, 6 combine.
 constexpr int kKernelsPerForward = 7;
+// Batches above kPermRowsT tokens (token tiles of 256, SM pairs) feed the gate_up GEMM its expert
+// rows from a copy of n2 in sorted-slot order, loaded by TMA boxes, instead of gathering them by
+// token index; the gate_up GEMM writes that copy itself before its first expert item.
+constexpr int kPermRowsT = 1024;
 // Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores (no fold kernel).
 constexpr int kRouterFmaT = 64;
 // Largest batch for which the down GEMM lets the combine kernel launch before it ends.
@@ -152,9 +161,19 @@ cudaError_t launch_gate_up_cvt(int bn, bool fp4, const GemmMaps& m, const Buffer
                               cudaStream_t s);
 cudaError_t launch_down_cvt(int bn, bool fp4, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
                            cudaStream_t s);
-// SM-pair (cta_group::2) down GEMM for token tiles of 256 (gemm_pair.cu).
+// The inputs of the sorted copy of n2 that the SM-pair gate_up GEMM writes: the layer input, the
+// expert branch's pre-norm weight (NULL in the experts-only mode, where n2 = x) and epsilon.
+struct PermIn {
+  const uint16_t* x;
+  const float* w2;
+  float eps;
+};
+
+// SM-pair (cta_group::2) gate_up and down GEMMs for token tiles of 256 (gemm_pair.cu).
 cudaError_t gemm_pair_set_smem_limits();
 int gemm_pair_max_clusters();
+cudaError_t launch_gate_up_pair(const GemmMaps& m, const Buffers& b, const PermIn& pin, int T, int full_layer, int grid,
+                                cudaStream_t s);
 cudaError_t launch_down_pair(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s);
 cudaError_t router_set_smem_limit();
 

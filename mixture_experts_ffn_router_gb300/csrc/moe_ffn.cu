@@ -140,7 +140,7 @@ Layout make_layout(const moe_ffn_config& c) {
   L.tile_off = take((E + 1) * 4);
   L.n_exp_tiles = take(4);
   L.done_ctr = take(4);
-  L.sched = take(8);
+  L.sched = take(12);
   L.status = take(4);
   L.exp_tiles = take(static_cast<size_t>(L.max_tiles) * 16);
   L.perm = take(S * 4);
@@ -183,6 +183,9 @@ struct moe_ffn_ctx {
   Buffers buf;
   // token-operand maps, one per token-tile width (box rows = BN): n1, h, h_dense
   CUtensorMap map_n1[4], map_h[4], map_hd[4];
+  // the experts' gate_up input in sorted-slot order (the y buffer), 128-row boxes (SM pairs: half
+  // a token tile per CTA)
+  CUtensorMap map_n2s_half;
   CUtensorMap map_wsplit;  // the router's split matrix, boxes of 64 x 128 rows
   // weight maps, re-encoded when the weight pointers change
   const void* cached_gate_up;
@@ -197,6 +200,8 @@ struct moe_ffn_ctx {
   bool cached_valid;
   CUtensorMap map_gate_up_q, map_down_q;  // converted experts: int8 rows or packed MXFP4 codes
   CUtensorMap map_gate_up, map_down, map_dense_gate, map_dense_up, map_dense_down;
+  // gate_up weights in 128-row boxes for the SM-pair GEMM (a CTA's 128 gate rows, then its up rows)
+  CUtensorMap map_gate_up_pair, map_dense_gate_pair, map_dense_up_pair;
   cudaEvent_t ev_start[kKernelsPerForward];
   cudaEvent_t ev_stop[kKernelsPerForward];
   int last_T;
@@ -276,12 +281,13 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
   b.h = reinterpret_cast<uint16_t*>(w + L.h);
   b.h_dense = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<uint16_t*>(w + L.h_dense) : nullptr;
   b.y = reinterpret_cast<uint16_t*>(w + L.y);
+  b.n2s = b.y;  // written and read by the SM-pair gate_up GEMM, then overwritten by the down GEMM
   b.d = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<float*>(w + L.d) : nullptr;
   b.wsplit = reinterpret_cast<uint16_t*>(w + L.wsplit);
   b.max_tiles = L.max_tiles;
 
   const uint64_t Tm = static_cast<uint64_t>(cfg->max_tokens);
-  bool ok = encode_bf16(&c->map_wsplit, b.wsplit, 3 * E, H, 128);
+  bool ok = encode_bf16(&c->map_wsplit, b.wsplit, 3 * E, H, 128) && encode_bf16(&c->map_n2s_half, b.n2s, Tm * K, H, 128);
   for (int k = 0; k < 4; ++k) {
     const uint32_t bn = 32u << k;
     ok = ok && encode_bf16(&c->map_h[k], b.h, Tm * K, I, bn);
@@ -360,15 +366,22 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
   if (!cvt) {
     c->map_gate_up_q = c->map_gate_up;
     c->map_down_q = c->map_down;
+    ok = ok && encode_bf16(&c->map_gate_up_pair, w->gate_up, static_cast<uint64_t>(E) * 2 * I, H, 128);
+  } else {
+    c->map_gate_up_pair = c->map_gate_up;
   }
   if (full)
     ok = ok && encode_bf16(&c->map_dense_gate, w->dense_gate, D, H, 64) &&
          encode_bf16(&c->map_dense_up, w->dense_up, D, H, 64) &&
-         encode_bf16(&c->map_dense_down, w->dense_down, H, D, 128);
+         encode_bf16(&c->map_dense_down, w->dense_down, H, D, 128) &&
+         encode_bf16(&c->map_dense_gate_pair, w->dense_gate, D, H, 128) &&
+         encode_bf16(&c->map_dense_up_pair, w->dense_up, D, H, 128);
   else {
     c->map_dense_gate = c->map_gate_up;
     c->map_dense_up = c->map_gate_up;
     c->map_dense_down = c->map_down;
+    c->map_dense_gate_pair = c->map_gate_up_pair;
+    c->map_dense_up_pair = c->map_gate_up_pair;
   }
   if (!ok) {
     c->cached_valid = false;
@@ -423,6 +436,9 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   const bool cvt = w->gate_up_q != nullptr || f4;
   rp.bn = cvt ? (T <= 128 ? 32 : 64) : choose_bn(T);
   rp.full_layer = full ? 1 : 0;
+  // Token tiles of 256 on SM pairs: the gate_up GEMM writes and reads the sorted copy of n2.
+  const bool perm_rows = !cvt && rp.bn == 256 && c->pair_clusters > 0;
+  rp.write_n2 = perm_rows ? 0 : 1;
   rp.eps = c->cfg.eps;
   rp.router_scale = c->cfg.router_scale;
 
@@ -465,15 +481,26 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
   const int grid_gu = static_cast<int>(items_gu < c->num_sms ? items_gu : c->num_sms);
   int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
-  // For token tiles of 256 (T above 1024) the down GEMM runs on SM pairs: M = 256 per pair of
-  // CTAs, half of each token tile in each CTA, so its B maps are the ones with 128-row boxes.
+  // For token tiles of 256 (T above 1024) both GEMMs run on SM pairs: M = 256 per pair of CTAs,
+  // half of each token tile in each CTA, so their B maps are the ones with 128-row boxes.
   const bool pairs = bn == 256 && c->pair_clusters > 0 && !cvt;
+  int grid_gu_launch = grid_gu;
   if (pairs) {
     grid_dn = 2 * c->pair_clusters;
+    grid_gu_launch = 2 * c->pair_clusters;
     dn.b_exp = c->map_h[2];
     dn.b_dense = c->map_hd[2];
+    gu.a_exp = c->map_gate_up_pair;
+    gu.a_dense0 = c->map_dense_gate_pair;
+    gu.a_dense1 = c->map_dense_up_pair;
+    gu.b_exp = c->map_n2s_half;
+    gu.b_dense = c->map_n1[2];
   }
 
+  PermIn pin;
+  pin.x = rp.x;
+  pin.w2 = full ? w->pre_ff_ln_2 : nullptr;
+  pin.eps = c->cfg.eps;
   cudaError_t e = cudaSuccess;
   for (int k = 0; k < kKernelsPerForward && e == cudaSuccess; ++k) {
     if (c->ev_start[k]) e = cudaEventRecord(c->ev_start[k], s);
@@ -487,8 +514,9 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4:
-        e = cvt ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, rp.full_layer, grid_gu, s)
-               : launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s);
+        e = cvt     ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, rp.full_layer, grid_gu, s)
+            : pairs ? launch_gate_up_pair(gu, c->buf, pin, T, rp.full_layer, grid_gu_launch, s)
+                    : launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s);
         break;
       case 5:
         e = cvt     ? launch_down_cvt(bn, f4, dn, c->buf, T, rp.full_layer, grid_dn, s)
@@ -546,9 +574,23 @@ int moe_ffn_set_kernel_events(moe_ffn_ctx* c, int kernel, void* start, void* sto
   return MOE_FFN_OK;
 }
 
+// The kernel slots a forward of T tokens launches, in launch order (see moe_ffn_set_kernel_events).
+static int slots_of(int T, int* slots) {
+  if (T == 0) return 0;
+  int n = 0;
+  for (int k = T > kRouterFmaT ? 0 : 1; k < kKernelsPerForward; ++k) slots[n++] = k;
+  return n;
+}
+
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* c, int T) {
   if (!c || T < 0) return MOE_FFN_EINVAL;
-  return T == 0 ? 0 : (T <= kRouterFmaT ? kKernelsPerForward - 1 : kKernelsPerForward);
+  int slots[kKernelsPerForward];
+  return slots_of(T, slots);
+}
+
+int moe_ffn_kernel_slots(const moe_ffn_ctx* c, int T, int* slots, int n_slots) {
+  if (!c || T < 0 || !slots || n_slots < kKernelsPerForward) return MOE_FFN_EINVAL;
+  return slots_of(T, slots);
 }
 
 }  // extern "C"

@@ -20,6 +20,7 @@ enum : uint32_t {
   kStatusBadSchedule = 1u << 5,    // a tile list larger than its buffer
   kStatusDrain = 1u << 6,          // an exit drain gave up waiting for work already in flight
   kStatusWaitItem = 1u << 7,       // a GEMM role gave up waiting for its next work item
+  kStatusWaitCopy = 1u << 8,       // a GEMM producer gave up waiting for the sorted copy of its inputs
 };
 
 constexpr unsigned long long kSpinLimitNs = 2000000000ull;  // 2 s
@@ -134,6 +135,32 @@ __device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity
       return false;
     }
   }
+}
+
+// Waits until the global counter *ctr reaches `target` (acquire at GPU scope), with the same bound
+// and failure reporting as mbar_wait_bounded. Only for counters that CTAs of the same grid raise,
+// where every CTA is resident at once.
+__device__ __forceinline__ bool counter_wait_bounded(const int* ctr, int target, volatile int* abort,
+                                                     unsigned int* status, uint32_t why) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if ((i & 15u) == 15u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kSpinLimitNs) {
+        *abort = 1;
+        atomicOr(status, why);
+        return false;
+      }
+    }
+  }
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA

@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
         *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
         b.sched[0] = 0;  // the GEMMs of this forward claim their work items from these counters
         b.sched[1] = 0;
+        b.sched[2] = 0;  // warps done with the sorted copy of n2 (SM-pair gate_up)
       }
     }
     __syncthreads();
@@ -336,9 +337,27 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     if (t >= p.T) break;
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
     const float inv = inv_s[warp * p.tpw + i];
-    // Expert-branch input n2 and dense-branch input n1.
+    // Expert-branch input n2 and dense-branch input n1 (n2 only where the gate_up GEMM gathers
+    // its rows by token index; above kPermRowsT tokens the gate_up GEMM writes them itself, in
+    // sorted-slot order).
     uint4* n2r = reinterpret_cast<uint4*>(b.n2 + static_cast<size_t>(t) * H);
-    if (p.full_layer) {
+    if (p.full_layer && !p.write_n2) {
+      uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
+#pragma unroll
+      for (int c = 0; c < 11; ++c) {
+        const float4 a0 = g_s[0][c][0][lane], a1 = g_s[0][c][1][lane];
+        const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint4 xc = __ldg(xr + lane + 32 * c);
+        const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
+        uint32_t o1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
+          o1[j] = pack_bf16(lo * g1[2 * j], hi * g1[2 * j + 1]);
+        }
+        n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      }
+    } else if (p.full_layer) {
       uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
 #pragma unroll
       for (int c = 0; c < 11; ++c) {
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
         n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
         n2r[lane + 32 * c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
       }
-    } else {
+    } else if (p.write_n2) {
 #pragma unroll
       for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = __ldg(xr + lane + 32 * c);
     }

@@ -73,6 +73,8 @@ def test_calls_that_need_no_device(lib):
     bad = B.make_config(7, 64)
     assert B.moe_ffn_workspace_bytes(bad) == 0
     assert lib.moe_ffn_kernels_per_forward(None, 4) == B.MOE_FFN_EINVAL
+    slots = (ctypes.c_int * 7)()
+    assert lib.moe_ffn_kernel_slots(None, 4, slots, 7) == B.MOE_FFN_EINVAL
     assert lib.moe_ffn_forward(None, None, 0, None, None, None) == B.MOE_FFN_EINVAL
     lib.moe_ffn_destroy(None)
 
@@ -160,6 +162,7 @@ def test_status_bits_match_the_kernels():
     assert macros and macros == snake
     assert macros == B.STATUS_BITS
     assert B.decode_status(0x41) == ["WAIT_FULL", "DRAIN"] and B.decode_status(0) == []
-    assert B.decode_status(0x102) == ["WAIT_EMPTY", "0x100"]
+    assert B.decode_status(0x102) == ["WAIT_EMPTY", "WAIT_COPY"]
+    assert B.decode_status(0x202) == ["WAIT_EMPTY", "0x200"]
     # The status word of a forward holds nothing else.
-    assert sum(macros.values()) == 0xff
+    assert sum(macros.values()) == 0x1ff

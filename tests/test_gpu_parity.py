@@ -76,6 +76,12 @@ def test_full_layer_sweep_sizes(T):
     _sampled_check(FULL, T, 400 + T, False, 32, "full T=%d" % T)
 
 
+def test_moe_only_prefill_sized():
+    # Experts only above 1024 tokens: token tiles of 256 on SM pairs, the expert input (x itself)
+    # copied into sorted-slot order, no shared-MLP group.
+    _sampled_check(MOE, 1100, 460, False, 32, "moe-only T=1100")
+
+
 def test_full_layer_prefill_uniform_4096():
     # The sweep's T=4096 point: uniform routing, so nearly every expert gets two token tiles of 256
     # (the second one partly filled).
