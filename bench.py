@@ -93,6 +93,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true",
                    help="default workload only: skip the T=4096 prefill leg of the line")
+    p.add_argument("--ep", action="store_true",
+                   help="expert parallel: each rank runs its contiguous share of the 128 experts on the same "
+                        "tokens, then the partial expert sums are all-reduced (NCCL) before the post norms")
     return p.parse_args(argv)
 
 
@@ -561,6 +564,102 @@ def measure(args, wl, weights, x, dev, world, rank, with_cpu, clocks, label):
             "kernels_us_note": "untimed breakdown pass, %d steps, events around every kernel" % n_b}
 
 
+def ep_exchange(part, dense, world, dist=None):
+    """The exchange step of the expert-parallel layer ("Porting a 128-expert MoE (Gemma-4 26B-A4B) to
+    AWS Inferentia2", section "The traceable trick": row-parallel down, then an all-reduce): the
+    ranks' fp32 partial expert sums are added in place (all-reduce, sum), and the shared MLP's
+    output, which rank 0 computes, is sent to every rank (broadcast). Both happen before
+    post_feedforward_layernorm_2, which is not linear."""
+    if world > 1:
+        if dist is None:
+            import torch.distributed as dist
+        dist.all_reduce(part, op=dist.ReduceOp.SUM)
+        dist.broadcast(dense, src=0)
+
+
+def ep_rank_step(rank, world, shard, exchange, finish, n_experts=E):
+    """One expert-parallel layer step of one rank: its experts (expert_range) and, on rank 0, the
+    shared MLP; the exchange; the rest of the block. shard(begin, end, with_dense) -> (part, dense
+    buffer); exchange(part, dense); finish(part, dense) -> output."""
+    from mixture_experts_ffn_router_gb300.binding import expert_range
+    b, e = expert_range(rank, world, n_experts)
+    part, dense = shard(b, e, rank == 0)
+    exchange(part, dense)
+    return finish(part, dense)
+
+
+def run_ep(args, wl):
+    import torch
+    from mixture_experts_ffn_router_gb300 import binding as B
+    from mixture_experts_ffn_router_gb300 import synth
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T = wl["T"]
+    if not wl["full"] or wl.get("layers", 1) != 1 or wl.get("int8") or wl.get("fp4"):
+        raise SystemExit("--ep runs the full layer with bf16 experts, one layer")
+    # Every rank draws the same layer and tokens (the same seeds): the router and the top-8 choice
+    # are replicated, the experts split.
+    w = synth.make_weights(seed=args.seed, device=dev, full_layer=True, skew=wl["skew"])
+    x = synth.make_x(T, seed=args.seed, device=dev)
+    m = B.MoeFFN(B.MOE_FFN_FULL_LAYER, T, device=local)
+    ws = B.weights_struct(w)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    part = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dense = torch.zeros((T, H), dtype=torch.float32, device=dev)
+    out = torch.empty_like(x)
+    import torch.distributed as dist
+
+    def shard(b, e, with_dense):
+        rc = B.moe_ffn_forward_shard(m.ctx, x.data_ptr(), T, ws, b, e, with_dense, part.data_ptr(),
+                                     dense.data_ptr() if with_dense else 0, s)
+        if rc != B.MOE_FFN_OK:
+            raise B.MoeFFNError("moe_ffn_forward_shard", rc)
+        return part, dense
+
+    def finish(p_, d_):
+        rc = B.moe_ffn_finish_shards(m.ctx, x.data_ptr(), T, ws, p_.data_ptr(), d_.data_ptr(), out.data_ptr(), s)
+        if rc != B.MOE_FFN_OK:
+            raise B.MoeFFNError("moe_ffn_finish_shards", rc)
+        return out
+
+    def step():
+        return ep_rank_step(rank, world, shard, lambda p_, d_: ep_exchange(p_, d_, world, dist), finish)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    rc, word = m.status()
+    if rc != B.MOE_FFN_OK:
+        raise RuntimeError("device status 0x%x after the timed steps" % word)
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    if rank == 0:
+        cfg = config_of(wl, world)
+        cfg["parallelism"] = "expert parallel over %d ranks (experts split, tokens and router replicated; " \
+                             "all-reduce of the partial expert sums, broadcast of the shared-MLP output)" % world
+        line = {"metric": METRIC, "value": T * args.steps / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": cfg, "impl": "ours-expert-parallel",
+                "gpu_launches": args.steps * (B.moe_ffn_kernels_per_forward(m.ctx, T) + 1)}
+        print(json.dumps(line), flush=True)
+    m.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_ours(args, wl):
     import torch
     from mixture_experts_ffn_router_gb300 import synth
@@ -633,6 +732,8 @@ def main(argv=None):
     wl = workload_of(args)
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.ep:
+        return run_ep(args, wl)
     return run_ours(args, wl)
 
 

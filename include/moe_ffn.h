@@ -151,7 +151,7 @@ typedef struct moe_ffn_views {
   const uint16_t* h;          /* [S, 704] bf16 gelu_tanh(gate) * up per sorted slot */
   const uint16_t* h_dense;    /* [T, 2112] bf16 shared-MLP activation (FULL_LAYER) */
   const uint16_t* y;          /* [S, 2816] bf16 weighted expert output per sorted slot */
-  const float* d;             /* [T, 2816] fp32 shared-MLP output (FULL_LAYER) */
+  const uint16_t* d;          /* [T, 2816] bf16 shared-MLP output (FULL_LAYER) */
   int T;                      /* tokens of that forward */
 } moe_ffn_views;
 
@@ -183,6 +183,41 @@ int moe_ffn_init(moe_ffn_ctx** ctx, const moe_ffn_config* cfg, void* workspace,
  * moe_ffn_device_status). */
 int moe_ffn_forward(moe_ffn_ctx* ctx, const void* x, int T, const moe_ffn_weights* w, void* out,
                     void* stream);
+
+/* Expert-parallel shard of one forward ("Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS
+ * Inferentia2", section "The traceable trick: compute all experts, mask to top-8": each rank owns a
+ * contiguous group of experts, e.g. 16 of 128 on 8 ranks, and the ranks' expert outputs are summed
+ * by an all-reduce). Every rank computes the router and the top-8 choice for all T tokens (the
+ * router weights are replicated, so all ranks choose the same experts without an exchange), then
+ * runs the grouped GEMMs over the experts [expert_begin, expert_end) only, and writes
+ *   moe_partial  device pointer, [T, 2816] fp32: for each token, the sum over its selected experts
+ *                in the range, in ascending expert id, of (routing weight x expert output), each
+ *                term rounded to bf16 as in moe_ffn_forward; 0 where none is in the range. This is
+ *                the expert branch before post_feedforward_layernorm_2, which is not linear, so
+ *                the ranks exchange and add these partials (an all-reduce sum) before it;
+ *   dense_out    with with_dense != 0 (FULL_LAYER only): device pointer, [T, 2816] fp32, the shared
+ *                MLP's output before post_feedforward_layernorm_1 (bf16 values widened); one rank
+ *                runs it. With with_dense == 0 it is not read and may be NULL.
+ * x, T and w are as for moe_ffn_forward (w must hold every field moe_ffn_forward needs). 0 <=
+ * expert_begin <= expert_end <= 128 (an empty range writes zeros). The outputs must not overlap x,
+ * each other or the workspace. Asynchronous on `stream`; the same errors as moe_ffn_forward, and
+ * MOE_FFN_EINVAL for a bad range or with_dense in MOE_FFN_MOE_ONLY mode. The workspace views hold
+ * this shard's routing (all experts) afterwards. */
+int moe_ffn_forward_shard(moe_ffn_ctx* ctx, const void* x, int T, const moe_ffn_weights* w, int expert_begin,
+                          int expert_end, int with_dense, float* moe_partial, float* dense_out, void* stream);
+
+/* The rest of the block after the shards' exchange: out = (x + RMSNorm(RMSNorm(dense;
+ * post_feedforward_layernorm_1) + RMSNorm(moe_sum; post_feedforward_layernorm_2);
+ * post_feedforward_layernorm)) x layer_scalar in FULL_LAYER mode (the same arithmetic as the end of
+ * moe_ffn_forward), out = moe_sum rounded to bf16 in MOE_FFN_MOE_ONLY mode.
+ *   moe_sum  device pointer, [T, 2816] fp32: the sum over all shards of moe_partial;
+ *   dense    device pointer, [T, 2816] fp32: the dense_out of the rank that ran the shared MLP
+ *            (FULL_LAYER; ignored and may be NULL in MOE_ONLY mode);
+ *   x        device pointer, [T, 2816] bf16, the layer input (FULL_LAYER);
+ *   out      device pointer, [T, 2816] bf16; must not overlap x, moe_sum or dense.
+ * Reads the norm weights and layer_scalar of w. Asynchronous on `stream`. */
+int moe_ffn_finish_shards(moe_ffn_ctx* ctx, const void* x, int T, const moe_ffn_weights* w, const float* moe_sum,
+                          const float* dense, void* out, void* stream);
 
 /* Fills *views with device pointers into the workspace (see moe_ffn_views). */
 int moe_ffn_workspace_view(const moe_ffn_ctx* ctx, moe_ffn_views* views);

@@ -84,6 +84,12 @@ def lib():
                                    ctypes.c_int]
         L.moe_ffn_forward.restype = ctypes.c_int
         L.moe_ffn_forward.argtypes = [_vp, _vp, ctypes.c_int, ctypes.POINTER(moe_ffn_weights), _vp, _vp]
+        L.moe_ffn_forward_shard.restype = ctypes.c_int
+        L.moe_ffn_forward_shard.argtypes = [_vp, _vp, ctypes.c_int, ctypes.POINTER(moe_ffn_weights), ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]
+        L.moe_ffn_finish_shards.restype = ctypes.c_int
+        L.moe_ffn_finish_shards.argtypes = [_vp, _vp, ctypes.c_int, ctypes.POINTER(moe_ffn_weights), _vp, _vp, _vp,
+                                            _vp]
         L.moe_ffn_workspace_view.restype = ctypes.c_int
         L.moe_ffn_workspace_view.argtypes = [_vp, ctypes.POINTER(moe_ffn_views)]
         L.moe_ffn_device_status.restype = ctypes.c_int
@@ -148,6 +154,27 @@ def moe_ffn_init(cfg: moe_ffn_config, workspace: int, workspace_bytes: int, devi
 
 def moe_ffn_forward(ctx: int, x: int, T: int, weights: moe_ffn_weights, out: int, stream: int) -> int:
     return lib().moe_ffn_forward(_vp(ctx), _vp(x), int(T), ctypes.byref(weights), _vp(out), _vp(stream))
+
+
+def moe_ffn_forward_shard(ctx: int, x: int, T: int, weights: moe_ffn_weights, expert_begin: int, expert_end: int,
+                          with_dense: bool, moe_partial: int, dense_out: int, stream: int) -> int:
+    return lib().moe_ffn_forward_shard(_vp(ctx), _vp(x), int(T), ctypes.byref(weights), int(expert_begin),
+                                       int(expert_end), 1 if with_dense else 0, _vp(moe_partial), _vp(dense_out),
+                                       _vp(stream))
+
+
+def moe_ffn_finish_shards(ctx: int, x: int, T: int, weights: moe_ffn_weights, moe_sum: int, dense: int, out: int,
+                          stream: int) -> int:
+    return lib().moe_ffn_finish_shards(_vp(ctx), _vp(x), int(T), ctypes.byref(weights), _vp(moe_sum), _vp(dense),
+                                       _vp(out), _vp(stream))
+
+
+def expert_range(rank: int, world: int, n_experts: int = N_EXPERTS):
+    """The contiguous experts [begin, end) that rank `rank` of `world` owns (equal shares, the first
+    n_experts % world ranks one more)."""
+    base, extra = divmod(n_experts, world)
+    begin = rank * base + min(rank, extra)
+    return begin, begin + base + (1 if rank < extra else 0)
 
 
 def moe_ffn_workspace_view(ctx: int) -> moe_ffn_views:
@@ -329,6 +356,36 @@ class MoeFFN:
         ws = weights if isinstance(weights, moe_ffn_weights) else weights_struct(weights)
         s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
         _check("moe_ffn_forward", moe_ffn_forward(self.ctx, x.data_ptr(), T, ws, out.data_ptr(), s))
+        return out
+
+    def forward_shard(self, x, weights, expert_begin, expert_end, with_dense, stream=None):
+        """One expert-parallel shard: (moe_partial, dense_out or None), fp32 [T, 2816] tensors."""
+        import torch
+        T = check_io(x)
+        ws = weights if isinstance(weights, moe_ffn_weights) else weights_struct(weights)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        part = torch.empty((T, HIDDEN), dtype=torch.float32, device=x.device)
+        dense = torch.empty((T, HIDDEN), dtype=torch.float32, device=x.device) if with_dense else None
+        _check("moe_ffn_forward_shard",
+               moe_ffn_forward_shard(self.ctx, x.data_ptr(), T, ws, expert_begin, expert_end, with_dense,
+                                     part.data_ptr(), dense.data_ptr() if dense is not None else 0, s))
+        return part, dense
+
+    def finish_shards(self, x, weights, moe_sum, dense, out=None, stream=None):
+        """The block's output from the summed shard partials (and the shared-MLP output)."""
+        import torch
+        T = check_io(x, out)
+        for name, t in (("moe_sum", moe_sum), ("dense", dense)):
+            if t is not None:
+                _check_type_size(name, t, torch.float32, T * HIDDEN)
+                _check_placement(name, t)
+        if out is None:
+            out = torch.empty_like(x)
+        ws = weights if isinstance(weights, moe_ffn_weights) else weights_struct(weights)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        _check("moe_ffn_finish_shards",
+               moe_ffn_finish_shards(self.ctx, x.data_ptr(), T, ws, moe_sum.data_ptr(),
+                                     dense.data_ptr() if dense is not None else 0, out.data_ptr(), s))
         return out
 
     def views(self) -> moe_ffn_views:

@@ -33,7 +33,7 @@
 // gate_up epilogue: TMEM lanes 0..63 hold gate, 64..127 up, of features f0..f0+63. The warps of
 // quarters q and q+2 hold gate and up of the same 32 features; each hands half of its columns to
 // the other through shared memory, and each then forms h = gelu_tanh(gate) * up for 16 columns.
-// down epilogue: y[slot] = w_slot * acc (bf16, sorted-slot order); the shared MLP writes d (fp32).
+// down epilogue: y[slot] = w_slot * acc (bf16, sorted-slot order); the shared MLP writes d (bf16).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -651,17 +651,17 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
           const int f0 = tile * kBM + 32 * q;
           uint8_t* stg = reinterpret_cast<uint8_t*>(xw) + q * 4096;
           if (it.dense) {
-            float* sd = reinterpret_cast<float*>(stg);  // [32 tokens][32 features]
+            uint16_t* sd = reinterpret_cast<uint16_t*>(stg);  // [32 tokens][32 features] bf16
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sd[j * 32 + lane] = v[j];
+            for (int j = 0; j < 32; ++j) sd[j * 32 + lane] = f32_to_bf16_rn(v[j]);
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int idx = lane + 32 * i, r = idx >> 3, c4 = idx & 7;
+            for (int i = 0; i < 4; ++i) {
+              const int idx = lane + 32 * i, r = idx >> 2, c8 = idx & 3;
               const int col = c * 32 + r;
               if (col < it.rows)
-                *reinterpret_cast<float4*>(b.d + static_cast<size_t>(it.row0 + col) * H + f0 + 4 * c4) =
-                    *reinterpret_cast<const float4*>(sd + r * 32 + 4 * c4);
+                *reinterpret_cast<uint4*>(b.d + static_cast<size_t>(it.row0 + col) * H + f0 + 8 * c8) =
+                    *reinterpret_cast<const uint4*>(sd + r * 32 + 8 * c8);
             }
             __syncwarp();
           } else {

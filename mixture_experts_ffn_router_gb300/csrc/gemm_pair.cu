@@ -482,8 +482,20 @@ __global__ void __launch_bounds__(PCfg<GATE_UP>::kThreads, 1)
           }
         }
         const int pos[K] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        // An expert-parallel shard computes only its experts: the other slots need no copy.
+        int ex[K] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (pin.e_lo > 0 || pin.e_hi < E) {
+          const int4 ea = __ldcg(reinterpret_cast<const int4*>(b.topk_idx + static_cast<size_t>(t) * K));
+          const int4 eb = __ldcg(reinterpret_cast<const int4*>(b.topk_idx + static_cast<size_t>(t) * K + 4));
+          ex[0] = ea.x; ex[1] = ea.y; ex[2] = ea.z; ex[3] = ea.w;
+          ex[4] = eb.x; ex[5] = eb.y; ex[6] = eb.z; ex[7] = eb.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < K; ++k) ex[k] = pin.e_lo;
+        }
 #pragma unroll
         for (int k = 0; k < K; ++k) {
+          if (ex[k] < pin.e_lo || ex[k] >= pin.e_hi) continue;
           if (pos[k] < 0 || pos[k] >= S) {
             if (lane == 0) atomicOr(b.status, kStatusBadIndex);
             continue;
@@ -559,17 +571,17 @@ __global__ void __launch_bounds__(PCfg<GATE_UP>::kThreads, 1)
           // The warp's 32 features x 32 token columns go through shared memory so that the global
           // stores are 16-byte vectors along the feature dimension.
           if (it.dense) {
-            float* sd = reinterpret_cast<float*>(stg);  // [32 tokens][32 features]
+            uint16_t* sd = reinterpret_cast<uint16_t*>(stg);  // [32 tokens][32 features] bf16
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sd[j * 32 + lane] = v[j];
+            for (int j = 0; j < 32; ++j) sd[j * 32 + lane] = f32_to_bf16_rn(v[j]);
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int idx = lane + 32 * u, r = idx >> 3, c4 = idx & 7;
+            for (int u = 0; u < 4; ++u) {
+              const int idx = lane + 32 * u, r = idx >> 2, c8 = idx & 3;
               const int col = c * 32 + r;
               if (col < it.rows)
-                *reinterpret_cast<float4*>(b.d + static_cast<size_t>(it.row0 + col) * H + f0 + 4 * c4) =
-                    *reinterpret_cast<const float4*>(sd + r * 32 + 4 * c4);
+                *reinterpret_cast<uint4*>(b.d + static_cast<size_t>(it.row0 + col) * H + f0 + 8 * c8) =
+                    *reinterpret_cast<const uint4*>(sd + r * 32 + 8 * c8);
             }
             __syncwarp();
           } else {
@@ -669,7 +681,7 @@ cudaError_t launch_gate_up_pair(const GemmMaps& m, const Buffers& b, const PermI
 }
 
 cudaError_t launch_down_pair(const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid, cudaStream_t s) {
-  const PermIn none = {nullptr, nullptr, 0.0f};
+  const PermIn none = {nullptr, nullptr, 0.0f, 0, 0};
   return launch_pdl_pair(grouped_gemm_pair_kernel<false>, dim3(grid), dim3(PCfg<false>::kThreads), PCfg<false>::kSmem,
                          s, m.a_exp, m.a_dense0, m.a_dense1, m.b_exp, m.b_dense, b, none, T, full_layer);
 }

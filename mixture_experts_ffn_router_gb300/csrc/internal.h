@@ -46,7 +46,7 @@ struct Buffers {
   uint16_t* h_dense;    // [Tm, 2112]
   uint16_t* y;          // [S, 2816] bf16
   uint16_t* n2s;        // [S, 2816] bf16: n2 rows in sorted-slot order (T > kPermRowsT), aliases y
-  float* d;             // [Tm, 2816]
+  uint16_t* d;          // [Tm, 2816] bf16
   unsigned int* status; // [1]
   uint16_t* wsplit;     // [3, 128, 2816] bf16: W_r * (1 + router_norm_w) as hi + mid + lo
   int max_tiles;
@@ -67,6 +67,7 @@ struct RouteParams {
   int bn;               // token-tile width of the grouped GEMMs
   int full_layer;
   int write_n2;         // the top-k kernel writes n2 (token order); else the gate_up GEMM writes n2s
+  int e_lo, e_hi;       // the experts whose token tiles the GEMMs compute: [0, 128), or a shard's
   float eps;
   float router_scale;
 };
@@ -81,6 +82,15 @@ struct CombineParams {
   int T;
   int full_layer;
   float eps;
+};
+
+// The end of an expert-parallel shard forward: the fp32 sum of each token's weighted expert
+// outputs over the experts [e_lo, e_hi), and optionally the shared-MLP output widened to fp32.
+struct ShardParams {
+  int T;
+  int e_lo, e_hi;
+  float* moe_out;    // [T, 2816]
+  float* dense_out;  // [T, 2816] or NULL
 };
 
 // Maps of one grouped GEMM launch. For gate_up: a_exp = gate_up rows, a_dense0/1 = dense gate/up,
@@ -149,6 +159,8 @@ cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p,
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_route_scatter(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_combine_shard(const ShardParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_finish(const CombineParams& p, const float* moe_sum, const float* dense, cudaStream_t s);
 
 // Grouped GEMMs (gemm.cu). `grid` CTAs persistent over the device-side tile list.
 cudaError_t launch_gate_up(int bn, const GemmMaps& m, const Buffers& b, int T, int full_layer, int grid,
@@ -167,6 +179,7 @@ struct PermIn {
   const uint16_t* x;
   const float* w2;
   float eps;
+  int e_lo, e_hi;  // only the slots of these experts are copied (a shard's range, or all)
 };
 
 // SM-pair (cta_group::2) gate_up and down GEMMs for token tiles of 256 (gemm_pair.cu).

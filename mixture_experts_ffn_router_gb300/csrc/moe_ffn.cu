@@ -151,7 +151,7 @@ Layout make_layout(const moe_ffn_config& c) {
   L.h = take(S * I * 2);
   L.h_dense = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * D * 2 : 0);
   L.y = take(S * H * 2);
-  L.d = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * H * 4 : 0);
+  L.d = take(c.mode == MOE_FFN_FULL_LAYER ? Tm * H * 2 : 0);
   L.wsplit = take(static_cast<size_t>(3) * E * H * 2);
   L.total = o;
   return L;
@@ -282,7 +282,7 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
   b.h_dense = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<uint16_t*>(w + L.h_dense) : nullptr;
   b.y = reinterpret_cast<uint16_t*>(w + L.y);
   b.n2s = b.y;  // written and read by the SM-pair gate_up GEMM, then overwritten by the down GEMM
-  b.d = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<float*>(w + L.d) : nullptr;
+  b.d = cfg->mode == MOE_FFN_FULL_LAYER ? reinterpret_cast<uint16_t*>(w + L.d) : nullptr;
   b.wsplit = reinterpret_cast<uint16_t*>(w + L.wsplit);
   b.max_tiles = L.max_tiles;
 
@@ -400,18 +400,24 @@ static int prepare_weights(moe_ffn_ctx* c, const moe_ffn_weights* w) {
   return MOE_FFN_OK;
 }
 
-int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights* w, void* out, void* stream) {
-  if (!c || !w) return MOE_FFN_EINVAL;
-  if (T < 0) return MOE_FFN_EINVAL;
-  if (T > c->cfg.max_tokens) return MOE_FFN_ETOOBIG;
-  if (T == 0) return MOE_FFN_OK;
-  if (!x || !out) return MOE_FFN_EINVAL;
-  if (!aligned16(x) || !aligned16(out)) return MOE_FFN_EALIGN;
-  const size_t io_bytes = static_cast<size_t>(T) * H * 2;
-  const uint8_t* xb = static_cast<const uint8_t*>(x);
-  uint8_t* ob = static_cast<uint8_t*>(out);
-  if ((ob < xb + io_bytes && xb < ob + io_bytes) || (ob < c->ws + c->ws_bytes && c->ws < ob + io_bytes))
-    return MOE_FFN_EINVAL;
+// An expert-parallel shard of one forward: the experts [e_lo, e_hi) only, the shared MLP if
+// with_dense, and the fp32 partial outputs instead of the block's output.
+struct Shard {
+  int e_lo, e_hi;
+  bool with_dense;
+  float* moe_out;
+  float* dense_out;
+};
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uint8_t* pa = static_cast<const uint8_t*>(a);
+  const uint8_t* pb = static_cast<const uint8_t*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+// The launch sequence of one forward (sh == NULL) or of one shard of it. Arguments are checked.
+static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights* w, void* out, void* stream,
+                       const Shard* sh) {
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return MOE_FFN_ECUDA;
   if (cur != c->device && cudaSetDevice(c->device) != cudaSuccess) return MOE_FFN_ECUDA;
@@ -419,6 +425,8 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   if (rc != MOE_FFN_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
+  // The GEMMs run the shared-MLP group in the full layer, except in a shard that leaves it out.
+  const int gemm_full = full && (!sh || sh->with_dense) ? 1 : 0;
 
   RouteParams rp;
   rp.x = static_cast<const uint16_t*>(x);
@@ -439,6 +447,8 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   // Token tiles of 256 on SM pairs: the gate_up GEMM writes and reads the sorted copy of n2.
   const bool perm_rows = !cvt && rp.bn == 256 && c->pair_clusters > 0;
   rp.write_n2 = perm_rows ? 0 : 1;
+  rp.e_lo = sh ? sh->e_lo : 0;
+  rp.e_hi = sh ? sh->e_hi : E;
   rp.eps = c->cfg.eps;
   rp.router_scale = c->cfg.router_scale;
 
@@ -474,7 +484,7 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   const int S = T * K;
   const int bn = rp.bn;
   const int ub_tiles = (S < E ? S : E) + S / bn;
-  const int nd = full ? (T + bn - 1) / bn : 0;
+  const int nd = gemm_full ? (T + bn - 1) / bn : 0;
   const int ma = cvt ? 1 : gate_up_tiles_per_item(bn, T);
   const long items_gu = static_cast<long>(ub_tiles) * ((I / 64 + ma - 1) / ma) +
                         static_cast<long>(nd) * ((D / 64 + ma - 1) / ma);
@@ -501,6 +511,14 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
   pin.x = rp.x;
   pin.w2 = full ? w->pre_ff_ln_2 : nullptr;
   pin.eps = c->cfg.eps;
+  pin.e_lo = rp.e_lo;
+  pin.e_hi = rp.e_hi;
+  ShardParams spar;
+  spar.T = T;
+  spar.e_lo = rp.e_lo;
+  spar.e_hi = rp.e_hi;
+  spar.moe_out = sh ? sh->moe_out : nullptr;
+  spar.dense_out = sh ? sh->dense_out : nullptr;
   cudaError_t e = cudaSuccess;
   for (int k = 0; k < kKernelsPerForward && e == cudaSuccess; ++k) {
     if (c->ev_start[k]) e = cudaEventRecord(c->ev_start[k], s);
@@ -514,22 +532,93 @@ int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights*
       case 2: e = launch_route_topk(rp, c->buf, s); break;
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4:
-        e = cvt     ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, rp.full_layer, grid_gu, s)
-            : pairs ? launch_gate_up_pair(gu, c->buf, pin, T, rp.full_layer, grid_gu_launch, s)
-                    : launch_gate_up(bn, gu, c->buf, T, rp.full_layer, grid_gu, s);
+        e = cvt     ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, gemm_full, grid_gu, s)
+            : pairs ? launch_gate_up_pair(gu, c->buf, pin, T, gemm_full, grid_gu_launch, s)
+                    : launch_gate_up(bn, gu, c->buf, T, gemm_full, grid_gu, s);
         break;
       case 5:
-        e = cvt     ? launch_down_cvt(bn, f4, dn, c->buf, T, rp.full_layer, grid_dn, s)
-            : pairs ? launch_down_pair(dn, c->buf, T, rp.full_layer, grid_dn, s)
-                    : launch_down(bn, dn, c->buf, T, rp.full_layer, grid_dn, s);
+        e = cvt     ? launch_down_cvt(bn, f4, dn, c->buf, T, gemm_full, grid_dn, s)
+            : pairs ? launch_down_pair(dn, c->buf, T, gemm_full, grid_dn, s)
+                    : launch_down(bn, dn, c->buf, T, gemm_full, grid_dn, s);
         break;
-      case 6: e = launch_combine(cp, c->buf, s); break;
+      case 6: e = sh ? launch_combine_shard(spar, c->buf, s) : launch_combine(cp, c->buf, s); break;
     }
     if (e == cudaSuccess && c->ev_stop[k]) e = cudaEventRecord(c->ev_stop[k], s);
   }
   if (e != cudaSuccess) return MOE_FFN_ECUDA;
   c->last_T = T;
   return MOE_FFN_OK;
+}
+
+int moe_ffn_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights* w, void* out, void* stream) {
+  if (!c || !w) return MOE_FFN_EINVAL;
+  if (T < 0) return MOE_FFN_EINVAL;
+  if (T > c->cfg.max_tokens) return MOE_FFN_ETOOBIG;
+  if (T == 0) return MOE_FFN_OK;
+  if (!x || !out) return MOE_FFN_EINVAL;
+  if (!aligned16(x) || !aligned16(out)) return MOE_FFN_EALIGN;
+  const size_t io_bytes = static_cast<size_t>(T) * H * 2;
+  if (overlaps(out, io_bytes, x, io_bytes) || overlaps(out, io_bytes, c->ws, c->ws_bytes)) return MOE_FFN_EINVAL;
+  return run_forward(c, x, T, w, out, stream, nullptr);
+}
+
+int moe_ffn_forward_shard(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights* w, int expert_begin,
+                          int expert_end, int with_dense, float* moe_partial, float* dense_out, void* stream) {
+  if (!c || !w) return MOE_FFN_EINVAL;
+  if (T < 0 || expert_begin < 0 || expert_end > E || expert_begin > expert_end) return MOE_FFN_EINVAL;
+  const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
+  if (with_dense && !full) return MOE_FFN_EINVAL;
+  if (T > c->cfg.max_tokens) return MOE_FFN_ETOOBIG;
+  if (T == 0) return MOE_FFN_OK;
+  if (!x || !moe_partial || (with_dense && !dense_out)) return MOE_FFN_EINVAL;
+  if (!aligned16(x) || !aligned16(moe_partial) || (with_dense && !aligned16(dense_out))) return MOE_FFN_EALIGN;
+  const size_t f_bytes = static_cast<size_t>(T) * H * 4, x_bytes = static_cast<size_t>(T) * H * 2;
+  if (overlaps(moe_partial, f_bytes, x, x_bytes) || overlaps(moe_partial, f_bytes, c->ws, c->ws_bytes))
+    return MOE_FFN_EINVAL;
+  if (with_dense && (overlaps(dense_out, f_bytes, x, x_bytes) || overlaps(dense_out, f_bytes, c->ws, c->ws_bytes) ||
+                     overlaps(dense_out, f_bytes, moe_partial, f_bytes)))
+    return MOE_FFN_EINVAL;
+  Shard sh;
+  sh.e_lo = expert_begin;
+  sh.e_hi = expert_end;
+  sh.with_dense = with_dense != 0;
+  sh.moe_out = moe_partial;
+  sh.dense_out = with_dense ? dense_out : nullptr;
+  return run_forward(c, x, T, w, nullptr, stream, &sh);
+}
+
+int moe_ffn_finish_shards(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weights* w, const float* moe_sum,
+                          const float* dense, void* out, void* stream) {
+  if (!c || !w) return MOE_FFN_EINVAL;
+  if (T < 0) return MOE_FFN_EINVAL;
+  if (T > c->cfg.max_tokens) return MOE_FFN_ETOOBIG;
+  if (T == 0) return MOE_FFN_OK;
+  const bool full = c->cfg.mode == MOE_FFN_FULL_LAYER;
+  if (!moe_sum || !out || (full && (!x || !dense || !w->post_ff_ln_1 || !w->post_ff_ln_2 || !w->post_ff_ln)))
+    return MOE_FFN_EINVAL;
+  if (!aligned16(moe_sum) || !aligned16(out) || (full && (!aligned16(x) || !aligned16(dense))) ||
+      (full && (!aligned16(w->post_ff_ln_1) || !aligned16(w->post_ff_ln_2) || !aligned16(w->post_ff_ln))))
+    return MOE_FFN_EALIGN;
+  const size_t io_bytes = static_cast<size_t>(T) * H * 2, f_bytes = static_cast<size_t>(T) * H * 4;
+  if (overlaps(out, io_bytes, moe_sum, f_bytes) || (full && (overlaps(out, io_bytes, x, io_bytes) ||
+                                                             overlaps(out, io_bytes, dense, f_bytes))))
+    return MOE_FFN_EINVAL;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_FFN_ECUDA;
+  if (cur != c->device && cudaSetDevice(c->device) != cudaSuccess) return MOE_FFN_ECUDA;
+  CombineParams cp;
+  cp.x = static_cast<const uint16_t*>(x);
+  cp.post_ff_ln_1 = w->post_ff_ln_1;
+  cp.post_ff_ln_2 = w->post_ff_ln_2;
+  cp.post_ff_ln = w->post_ff_ln;
+  cp.layer_scalar = w->layer_scalar;
+  cp.out = static_cast<uint16_t*>(out);
+  cp.T = T;
+  cp.full_layer = full ? 1 : 0;
+  cp.eps = c->cfg.eps;
+  return launch_finish(cp, moe_sum, full ? dense : nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_FFN_OK
+             : MOE_FFN_ECUDA;
 }
 
 int moe_ffn_workspace_view(const moe_ffn_ctx* c, moe_ffn_views* v) {

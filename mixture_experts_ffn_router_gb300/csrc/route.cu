@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
       for (int j = 0; j < 4; ++j) {
         const int ee = lane * 4 + j;
         cnt[j] = part_s[0][ee] + part_s[1][ee];
-        nt[j] = (cnt[j] + p.bn - 1) / p.bn;
+        // Token tiles only for the experts this forward computes (all of them, or a shard's range).
+        nt[j] = (ee >= p.e_lo && ee < p.e_hi) ? (cnt[j] + p.bn - 1) / p.bn : 0;
         cs += cnt[j];
         ts += nt[j];
       }
@@ -463,6 +464,52 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
   return s;
 }
 
+// The block's output for 8 features f..f+7 of one token (a CTA per token, kCombineThreads threads
+// of 8 features): in the full layer, RMSNorm(d; post_feedforward_layernorm_1) +
+// RMSNorm(moe; post_feedforward_layernorm_2), normalised by post_feedforward_layernorm, plus the
+// residual x, times layer_scalar; in the experts-only mode the expert sum itself. bf16.
+__device__ __forceinline__ uint4 block_output(const CombineParams& p, const float (&dv)[8], const float (&moe)[8],
+                                              const uint4 xv, int f, float2* red) {
+  if (!p.full_layer)
+    return make_uint4(pack_bf16(moe[0], moe[1]), pack_bf16(moe[2], moe[3]), pack_bf16(moe[4], moe[5]),
+                      pack_bf16(moe[6], moe[7]));
+  float sd = 0.0f, sm = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sd = fmaf(dv[j], dv[j], sd);
+    sm = fmaf(moe[j], moe[j], sm);
+  }
+  const float2 r = block_sum2(make_float2(sd, sm), red);
+  const float inv_d = 1.0f / sqrtf(r.x / static_cast<float>(H) + p.eps);
+  const float inv_m = 1.0f / sqrtf(r.y / static_cast<float>(H) + p.eps);
+  const float4 g1a = *reinterpret_cast<const float4*>(p.post_ff_ln_1 + f);
+  const float4 g1b = *reinterpret_cast<const float4*>(p.post_ff_ln_1 + f + 4);
+  const float4 g2a = *reinterpret_cast<const float4*>(p.post_ff_ln_2 + f);
+  const float4 g2b = *reinterpret_cast<const float4*>(p.post_ff_ln_2 + f + 4);
+  const float g1[8] = {g1a.x, g1a.y, g1a.z, g1a.w, g1b.x, g1b.y, g1b.z, g1b.w};
+  const float g2[8] = {g2a.x, g2a.y, g2a.z, g2a.w, g2b.x, g2b.y, g2b.z, g2b.w};
+  float sv[8];
+  float ss = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sv[j] = dv[j] * inv_d * (1.0f + g1[j]) + moe[j] * inv_m * (1.0f + g2[j]);
+    ss = fmaf(sv[j], sv[j], ss);
+  }
+  const float inv_s = 1.0f / sqrtf(block_sum2(make_float2(ss, 0.0f), red).x / static_cast<float>(H) + p.eps);
+  const float4 g3a = *reinterpret_cast<const float4*>(p.post_ff_ln + f);
+  const float4 g3b = *reinterpret_cast<const float4*>(p.post_ff_ln + f + 4);
+  const float g3[8] = {g3a.x, g3a.y, g3a.z, g3a.w, g3b.x, g3b.y, g3b.z, g3b.w};
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  uint32_t ow[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = (bf16_lo(xw[j]) + sv[2 * j] * inv_s * (1.0f + g3[2 * j])) * p.layer_scalar;
+    const float hi = (bf16_hi(xw[j]) + sv[2 * j + 1] * inv_s * (1.0f + g3[2 * j + 1])) * p.layer_scalar;
+    ow[j] = pack_bf16(lo, hi);
+  }
+  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
 // One CTA per token, 8 features per thread. Every load that does not depend on another is issued
 // before the first use: the token's 8 slot positions, then its 8 rows of y, d and x, so the CTA
 // waits for memory about twice (positions, then rows) rather than once per load.
@@ -477,10 +524,13 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(CombinePara
   float dv[8];
   uint4 xv = make_uint4(0u, 0u, 0u, 0u);
   if (p.full_layer) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(b.d + static_cast<size_t>(t) * H + f));
-    const float4 c = __ldcs(reinterpret_cast<const float4*>(b.d + static_cast<size_t>(t) * H + f + 4));
-    dv[0] = a.x; dv[1] = a.y; dv[2] = a.z; dv[3] = a.w;
-    dv[4] = c.x; dv[5] = c.y; dv[6] = c.z; dv[7] = c.w;
+    const uint4 dd = __ldcs(reinterpret_cast<const uint4*>(b.d + static_cast<size_t>(t) * H + f));
+    const uint32_t d4[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      dv[2 * j] = bf16_lo(d4[j]);
+      dv[2 * j + 1] = bf16_hi(d4[j]);
+    }
     xv = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + f);
   }
   int pos[K] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
@@ -508,51 +558,90 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(CombinePara
       moe[2 * j + 1] += bf16_hi(w4[j]);
     }
   }
-  uint4 o;
-  if (!p.full_layer) {
-    o = make_uint4(pack_bf16(moe[0], moe[1]), pack_bf16(moe[2], moe[3]), pack_bf16(moe[4], moe[5]),
-                   pack_bf16(moe[6], moe[7]));
-  } else {
-    float sd = 0.0f, sm = 0.0f;
+  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H + f) = block_output(p, dv, moe, xv, f, red);
+}
+
+// ------------------------------------------------------------------------------------------
+// Expert-parallel shards ("Porting a 128-expert MoE (Gemma-4 26B-A4B) to AWS Inferentia2", section
+// "The traceable trick": each rank owns a contiguous group of experts and the ranks' expert
+// outputs are summed). A shard forward ends with combine_shard_kernel: per token, the sum of its
+// weighted expert outputs over the slots whose expert lies in [e_lo, e_hi), in ascending expert
+// id, in fp32 (the block's expert branch before post_feedforward_layernorm_2, which is not linear,
+// so the ranks add these partials before it); and, on the rank that ran the shared MLP, its
+// output d widened to fp32. finish_kernel then takes the summed partials and d and applies the
+// rest of the block with the combine's own arithmetic (block_output).
+__global__ void __launch_bounds__(kCombineThreads, 3) combine_shard_kernel(ShardParams p, Buffers b) {
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int f = tid * 8;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int4 pa = *reinterpret_cast<const int4*>(b.slot_pos + static_cast<size_t>(t) * K);
+  const int4 pb = *reinterpret_cast<const int4*>(b.slot_pos + static_cast<size_t>(t) * K + 4);
+  const int4 ea = *reinterpret_cast<const int4*>(b.topk_idx + static_cast<size_t>(t) * K);
+  const int4 eb = *reinterpret_cast<const int4*>(b.topk_idx + static_cast<size_t>(t) * K + 4);
+  const int pos[K] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+  const int ex[K] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+  const int n_slots = p.T * K;
+  float moe[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      sd = fmaf(dv[j], dv[j], sd);
-      sm = fmaf(moe[j], moe[j], sm);
-    }
-    const float2 r = block_sum2(make_float2(sd, sm), red);
-    const float inv_d = 1.0f / sqrtf(r.x / static_cast<float>(H) + p.eps);
-    const float inv_m = 1.0f / sqrtf(r.y / static_cast<float>(H) + p.eps);
-    const float4 g1a = *reinterpret_cast<const float4*>(p.post_ff_ln_1 + f);
-    const float4 g1b = *reinterpret_cast<const float4*>(p.post_ff_ln_1 + f + 4);
-    const float4 g2a = *reinterpret_cast<const float4*>(p.post_ff_ln_2 + f);
-    const float4 g2b = *reinterpret_cast<const float4*>(p.post_ff_ln_2 + f + 4);
-    const float g1[8] = {g1a.x, g1a.y, g1a.z, g1a.w, g1b.x, g1b.y, g1b.z, g1b.w};
-    const float g2[8] = {g2a.x, g2a.y, g2a.z, g2a.w, g2b.x, g2b.y, g2b.z, g2b.w};
-    float sv[8];
-    float ss = 0.0f;
+  for (int j = 0; j < 8; ++j) moe[j] = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      sv[j] = dv[j] * inv_d * (1.0f + g1[j]) + moe[j] * inv_m * (1.0f + g2[j]);
-      ss = fmaf(sv[j], sv[j], ss);
+  for (int k = 0; k < K; ++k) {
+    if (ex[k] < p.e_lo || ex[k] >= p.e_hi) continue;
+    if (pos[k] < 0 || pos[k] >= n_slots) {
+      if (tid == 0) atomicOr(b.status, kStatusBadIndex);
+      continue;
     }
-    const float inv_s = 1.0f / sqrtf(block_sum2(make_float2(ss, 0.0f), red).x / static_cast<float>(H) + p.eps);
-    const float4 g3a = *reinterpret_cast<const float4*>(p.post_ff_ln + f);
-    const float4 g3b = *reinterpret_cast<const float4*>(p.post_ff_ln + f + 4);
-    const float g3[8] = {g3a.x, g3a.y, g3a.z, g3a.w, g3b.x, g3b.y, g3b.z, g3b.w};
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    uint32_t ow[4];
+    const uint4 yv = __ldcs(reinterpret_cast<const uint4*>(b.y + static_cast<size_t>(pos[k]) * H + f));
+    const uint32_t w4[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float lo = (bf16_lo(xw[j]) + sv[2 * j] * inv_s * (1.0f + g3[2 * j])) * p.layer_scalar;
-      const float hi = (bf16_hi(xw[j]) + sv[2 * j + 1] * inv_s * (1.0f + g3[2 * j + 1])) * p.layer_scalar;
-      ow[j] = pack_bf16(lo, hi);
+      moe[2 * j] += bf16_lo(w4[j]);
+      moe[2 * j + 1] += bf16_hi(w4[j]);
     }
-    o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
   }
-  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H + f) = o;
+  float4* mo = reinterpret_cast<float4*>(p.moe_out + static_cast<size_t>(t) * H + f);
+  mo[0] = make_float4(moe[0], moe[1], moe[2], moe[3]);
+  mo[1] = make_float4(moe[4], moe[5], moe[6], moe[7]);
+  if (p.dense_out) {
+    const uint4 dd = __ldcs(reinterpret_cast<const uint4*>(b.d + static_cast<size_t>(t) * H + f));
+    float4* dof = reinterpret_cast<float4*>(p.dense_out + static_cast<size_t>(t) * H + f);
+    dof[0] = make_float4(bf16_lo(dd.x), bf16_hi(dd.x), bf16_lo(dd.y), bf16_hi(dd.y));
+    dof[1] = make_float4(bf16_lo(dd.z), bf16_hi(dd.z), bf16_lo(dd.w), bf16_hi(dd.w));
+  }
+}
+
+__global__ void __launch_bounds__(kCombineThreads, 3) finish_kernel(CombineParams p, const float* moe_sum,
+                                                                    const float* dense) {
+  __shared__ float2 red[kCombineThreads / 32];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int f = tid * 8;
+  pdl_wait();
+  pdl_launch_dependents();
+  const float4* mi = reinterpret_cast<const float4*>(moe_sum + static_cast<size_t>(t) * H + f);
+  const float4 m0 = mi[0], m1 = mi[1];
+  const float moe[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float dv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+  if (p.full_layer) {
+    const float4* di = reinterpret_cast<const float4*>(dense + static_cast<size_t>(t) * H + f);
+    const float4 d0 = di[0], d1 = di[1];
+    dv[0] = d0.x; dv[1] = d0.y; dv[2] = d0.z; dv[3] = d0.w;
+    dv[4] = d1.x; dv[5] = d1.y; dv[6] = d1.z; dv[7] = d1.w;
+    xv = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H + f);
+  }
+  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * H + f) = block_output(p, dv, moe, xv, f, red);
 }
 
 }  // namespace
+
+cudaError_t launch_combine_shard(const ShardParams& p, const Buffers& b, cudaStream_t s) {
+  return launch_pdl(combine_shard_kernel, dim3(p.T), dim3(kCombineThreads), 0, s, p, b);
+}
+
+cudaError_t launch_finish(const CombineParams& p, const float* moe_sum, const float* dense, cudaStream_t s) {
+  return launch_pdl(finish_kernel, dim3(p.T), dim3(kCombineThreads), 0, s, p, moe_sum, dense);
+}
 
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s) {
   const int tb = 8 * p.tpw;

@@ -100,3 +100,15 @@ def test_forward_io_checks():
         B.check_io(x, torch.empty(5, H, device="meta"))
     with pytest.raises(ValueError, match="CUDA tensor"):
         B.check_io(torch.empty(0, H, dtype=torch.bfloat16, device="meta"))
+
+
+def test_expert_ranges_cover_the_experts_once():
+    # The contiguous expert groups of the expert-parallel shards ("The traceable trick": rank r of 8
+    # owns experts 16 r .. 16 r + 15): every expert exactly once, sizes within one of each other.
+    assert [B.expert_range(r, 8) for r in range(8)] == [(16 * r, 16 * r + 16) for r in range(8)]
+    for world in (1, 2, 3, 8, 16, 128):
+        rs = [B.expert_range(r, world) for r in range(world)]
+        assert rs[0][0] == 0 and rs[-1][1] == 128
+        assert all(rs[i][1] == rs[i + 1][0] for i in range(world - 1))
+        sizes = [e - b for b, e in rs]
+        assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 1

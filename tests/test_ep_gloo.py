@@ -11,6 +11,9 @@ ranks' partial expert outputs with an all-reduce. These tests pin that decomposi
   sum through the post norms. The exchange has to come before post_feedforward_layernorm_2: the
   same norms applied per rank and summed afterwards give a different block.
 * With world size 2 on gloo, an all-reduce of the two ranks' partials reproduces the output.
+* bench.py's expert-parallel step (its expert ranges, the all-reduce of the partials and the
+  broadcast of rank 0's shared-MLP output, then the finishing arithmetic), run by two gloo ranks
+  with oracle shards, reproduces the output on both ranks.
 """
 import os
 import socket
@@ -149,6 +152,51 @@ def test_expert_parallel_all_reduce_on_gloo():
     shape = tiny.SMALL
     d = tiny.dims_of(shape, full_layer=True)
     x, w = tiny.case(shape, 9, 57, weight_std=0.2)
+    full = oracle.forward(d, x, w, want=("out",))
+    for r in (0, 1):
+        np.testing.assert_allclose(res[r], full["out"], rtol=1e-12, atol=1e-12)
+
+
+def _bench_rank_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import bench
+    from tests import tiny as tn
+    import oracle as orc
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    shape = tn.SMALL
+    d = tn.dims_of(shape, full_layer=True)
+    x, w = tn.case(shape, 7, 61, weight_std=0.2)
+
+    def shard(b, e, with_dense):
+        r = orc.forward(d, x, _shard_weights(w, range(b, e)), want=("moe", "dense"))
+        part = torch.from_numpy(r["moe"].copy())
+        dense = torch.from_numpy(r["dense"].copy()) if with_dense else torch.zeros_like(part)
+        return part, dense
+
+    out = bench.ep_rank_step(rank, world, shard, lambda p, dd: bench.ep_exchange(p, dd, world, dist),
+                             lambda p, dd: _block_from_branches(p.numpy(), dd.numpy(), x, w, d["eps"]),
+                             n_experts=shape["n_experts"])
+    q.put((rank, out))
+    dist.destroy_process_group()
+
+
+def test_bench_expert_parallel_step_on_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bench_rank_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=180) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    shape = tiny.SMALL
+    d = tiny.dims_of(shape, full_layer=True)
+    x, w = tiny.case(shape, 7, 61, weight_std=0.2)
     full = oracle.forward(d, x, w, want=("out",))
     for r in (0, 1):
         np.testing.assert_allclose(res[r], full["out"], rtol=1e-12, atol=1e-12)
