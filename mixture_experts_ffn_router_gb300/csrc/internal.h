@@ -149,6 +149,11 @@ constexpr int kKernelsPerForward = 7;
 // rows from a copy of n2 in sorted-slot order, loaded by TMA boxes, instead of gathering them by
 // token index; the gate_up GEMM writes that copy itself before its first expert item.
 constexpr int kPermRowsT = 1024;
+// The gate_up GEMM runs on SM pairs (with the sorted copy of n2) above kPairGateUpT tokens; from
+// kPermRowsT to kPairGateUpT it stays on single SMs with gathered token rows, where the copy's cost
+// is not yet repaid. Layer time, uniform routing, single SMs vs pairs: T = 1500 372.5 vs 384.3 us,
+// 2048 402.9 vs 415.2, 2560 448.1 vs 456.0, 3072 474.8 vs 479.3, 4096 636.0 vs 621.6.
+constexpr int kPairGateUpT = 3072;
 // Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores (no fold kernel).
 constexpr int kRouterFmaT = 64;
 // Largest batch for which the down GEMM lets the combine kernel launch before it ends.

@@ -444,8 +444,9 @@ static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weigh
   const bool cvt = w->gate_up_q != nullptr || f4;
   rp.bn = cvt ? (T <= 128 ? 32 : 64) : choose_bn(T);
   rp.full_layer = full ? 1 : 0;
-  // Token tiles of 256 on SM pairs: the gate_up GEMM writes and reads the sorted copy of n2.
-  const bool perm_rows = !cvt && rp.bn == 256 && c->pair_clusters > 0;
+  // Token tiles of 256 on SM pairs (above kPairGateUpT tokens): the gate_up GEMM writes and reads
+  // the sorted copy of n2.
+  const bool perm_rows = !cvt && rp.bn == 256 && c->pair_clusters > 0 && T > kPairGateUpT;
   rp.write_n2 = perm_rows ? 0 : 1;
   rp.e_lo = sh ? sh->e_lo : 0;
   rp.e_hi = sh ? sh->e_hi : E;
@@ -491,15 +492,19 @@ static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weigh
   const long items_dn = static_cast<long>(ub_tiles) * (H / 128) + static_cast<long>(nd) * (H / 128);
   const int grid_gu = static_cast<int>(items_gu < c->num_sms ? items_gu : c->num_sms);
   int grid_dn = static_cast<int>(items_dn < c->num_sms ? items_dn : c->num_sms);
-  // For token tiles of 256 (T above 1024) both GEMMs run on SM pairs: M = 256 per pair of CTAs,
-  // half of each token tile in each CTA, so their B maps are the ones with 128-row boxes.
+  // For token tiles of 256 (T above 1024) the down GEMM runs on SM pairs, and above kPairGateUpT
+  // tokens the gate_up GEMM too: M = 256 per pair of CTAs, half of each token tile in each CTA, so
+  // their B maps are the ones with 128-row boxes.
   const bool pairs = bn == 256 && c->pair_clusters > 0 && !cvt;
+  const bool pairs_gu = perm_rows;
   int grid_gu_launch = grid_gu;
   if (pairs) {
     grid_dn = 2 * c->pair_clusters;
-    grid_gu_launch = 2 * c->pair_clusters;
     dn.b_exp = c->map_h[2];
     dn.b_dense = c->map_hd[2];
+  }
+  if (pairs_gu) {
+    grid_gu_launch = 2 * c->pair_clusters;
     gu.a_exp = c->map_gate_up_pair;
     gu.a_dense0 = c->map_dense_gate_pair;
     gu.a_dense1 = c->map_dense_up_pair;
@@ -533,7 +538,7 @@ static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weigh
       case 3: e = launch_route_scatter(rp, c->buf, s); break;
       case 4:
         e = cvt     ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, gemm_full, grid_gu, s)
-            : pairs ? launch_gate_up_pair(gu, c->buf, pin, T, gemm_full, grid_gu_launch, s)
+            : pairs_gu ? launch_gate_up_pair(gu, c->buf, pin, T, gemm_full, grid_gu_launch, s)
                     : launch_gate_up(bn, gu, c->buf, T, gemm_full, grid_gu, s);
         break;
       case 5:

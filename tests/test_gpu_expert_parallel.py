@@ -15,7 +15,8 @@ Checks, on the same seeded inputs as the oracle:
   * one shard holding all 128 experts gives the unsharded forward bit for bit;
   * argument errors.
 Sizes cover decode tiles (T=64), single-SM 128-token tiles (T=300), SM-pair prefill tiles with
-skewed routing (T=1500) and the experts-only mode.
+skewed routing (T=3200: the gate_up GEMM copies only the shard's slots into sorted order) and the
+experts-only mode.
 """
 import numpy as np
 import pytest
@@ -63,7 +64,7 @@ def _run_shards(m, x, w, n):
 
 
 @pytest.mark.parametrize("mode,T,n,seed,skew", [(FULL, 64, 8, 2001, False), (FULL, 300, 2, 2002, False),
-                                                (FULL, 1500, 8, 2003, True), (MOE, 200, 4, 2004, False)])
+                                                (FULL, 3200, 8, 2003, True), (MOE, 200, 4, 2004, False)])
 def test_shards_sum_to_the_block(mode, T, n, seed, skew):
     x, w = G.make_case(mode, T, seed, skew=skew)
     m = B.MoeFFN(mode, T)
@@ -99,7 +100,7 @@ def test_shards_sum_to_the_block(mode, T, n, seed, skew):
     assert frob < 2e-3, "sharded vs unsharded rel Frobenius %.3e" % frob
 
 
-@pytest.mark.parametrize("mode,T", [(FULL, 64), (FULL, 1100), (MOE, 33)])
+@pytest.mark.parametrize("mode,T", [(FULL, 64), (FULL, 1100), (FULL, 3100), (MOE, 33)])
 def test_one_shard_of_all_experts_is_the_forward(mode, T):
     x, w = G.make_case(mode, T, 2100 + T)
     m = B.MoeFFN(mode, T)

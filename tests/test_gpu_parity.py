@@ -76,10 +76,12 @@ def test_full_layer_sweep_sizes(T):
     _sampled_check(FULL, T, 400 + T, False, 32, "full T=%d" % T)
 
 
-def test_moe_only_prefill_sized():
-    # Experts only above 1024 tokens: token tiles of 256 on SM pairs, the expert input (x itself)
-    # copied into sorted-slot order, no shared-MLP group.
-    _sampled_check(MOE, 1100, 460, False, 32, "moe-only T=1100")
+@pytest.mark.parametrize("T", [1100, 3100])
+def test_moe_only_prefill_sized(T):
+    # Experts only above 1024 tokens: token tiles of 256, the down GEMM on SM pairs; above 3072 the
+    # gate_up GEMM too, with the expert input (x itself) copied into sorted-slot order and no
+    # shared-MLP items to run meanwhile.
+    _sampled_check(MOE, T, 460, False, 32, "moe-only T=%d" % T)
 
 
 def test_full_layer_prefill_uniform_4096():
