@@ -96,6 +96,14 @@ def test_full_layer_max_sweep_16384():
     _sampled_check(FULL, 16384, 500, False, 24, "full T=16384")
 
 
+@pytest.mark.slow
+def test_full_layer_max_tokens_65536():
+    # The largest batch a context accepts (MOE_FFN_MAX_TOKENS_LIMIT): 256 chunks of 256 tokens for
+    # the counting sort, 524,288 slots, a 2.95 GB sorted copy of n2 in the y buffer.
+    run, _ = _sampled_check(FULL, 65536, 510, False, 16, "full T=65536")
+    assert run.counts.sum() == 65536 * 8
+
+
 def test_all_tokens_identical_pick_the_same_experts():
     # Identical tokens choose the same 8 experts: 8 experts get all T tokens (several token tiles
     # each), the other 120 get none.
