@@ -406,7 +406,7 @@ def measure(args, wl, weights, x, dev, world, rank, with_cpu, clocks, label):
     # Slots a forward of this size leaves empty are not reported.
     used = B.moe_ffn_kernel_slots(m.ctx, T)
     nk = len(used)
-    kernel_us = {B.KERNEL_NAMES[k]: float(np.mean([bd[i][k][0].elapsed_time(bd[i][k][1]) for i in range(n_b)]) * 1e3)
+    kernel_us = {B.slot_name(k, T): float(np.mean([bd[i][k][0].elapsed_time(bd[i][k][1]) for i in range(n_b)]) * 1e3)
                  for k in used}
     gemms = {"gate_up_gemm": B.KERNEL_NAMES.index("gate_up_gemm"), "down_gemm": B.KERNEL_NAMES.index("down_gemm")}
     dom = max(gemms, key=lambda n: kernel_us[n])

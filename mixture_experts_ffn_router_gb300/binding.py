@@ -35,6 +35,16 @@ def decode_status(word: int) -> list:
 
 
 KERNEL_NAMES = ("router_prep", "router_logits", "route_topk", "route_scatter", "gate_up_gemm", "down_gemm", "combine")
+# Forwards of at most this many tokens run the whole routing front end (router sums, top-k,
+# counting sort) as one kernel in slot 1; slots 0, 2 and 3 then launch nothing.
+ROUTE_SMALL_T = 64
+
+
+def slot_name(slot: int, T: int) -> str:
+    """Name of the kernel a forward of T tokens launches in kernel slot `slot`."""
+    if slot == 1 and T <= ROUTE_SMALL_T:
+        return "route_small"
+    return KERNEL_NAMES[slot]
 
 _vp = ctypes.c_void_p
 

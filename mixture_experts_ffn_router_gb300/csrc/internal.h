@@ -35,6 +35,7 @@ struct Buffers {
   int32_t* done_ctr;    // [1]
   int32_t* sched;       // [3] work-item counters of the gate_up and down GEMMs, and the count of
                         // warps that finished the sorted copy of n2 (all zeroed by top-k)
+  int32_t* small_ctr;   // [8] tickets of the small-batch routing kernel (zero between forwards)
   int4* exp_tiles;      // [max_tiles] (expert, first sorted row, rows, 0), grouped by expert
   int32_t* tile_off;    // [129] index of each expert's first token tile in exp_tiles
   int32_t* perm;        // [S]
@@ -45,7 +46,7 @@ struct Buffers {
   uint16_t* h;          // [S, 704]
   uint16_t* h_dense;    // [Tm, 2112]
   uint16_t* y;          // [S, 2816] bf16
-  uint16_t* n2s;        // [S, 2816] bf16: n2 rows in sorted-slot order (T > kPermRowsT), aliases y
+  uint16_t* n2s;        // [S, 2816] bf16: n2 rows in sorted-slot order (T > kPairGateUpT), aliases y
   uint16_t* d;          // [Tm, 2816] bf16
   unsigned int* status; // [1]
   uint16_t* wsplit;     // [3, 128, 2816] bf16: W_r * (1 + router_norm_w) as hi + mid + lo
@@ -145,20 +146,19 @@ inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block
 // Kernel slots of one forward (events, breakdown): 0 router prep, 1 router logits, 2 top-k,
 // 3 scatter, 4 gate_up, 5 down, 6 combine.
 constexpr int kKernelsPerForward = 7;
-// Batches above kPermRowsT tokens (token tiles of 256, SM pairs) feed the gate_up GEMM its expert
-// rows from a copy of n2 in sorted-slot order, loaded by TMA boxes, instead of gathering them by
-// token index; the gate_up GEMM writes that copy itself before its first expert item.
-constexpr int kPermRowsT = 1024;
-// The gate_up GEMM runs on SM pairs (with the sorted copy of n2) above kPairGateUpT tokens; from
-// kPermRowsT to kPairGateUpT it stays on single SMs with gathered token rows, where the copy's cost
+// Above kPairGateUpT tokens (token tiles of 256) the gate_up GEMM runs on SM pairs and takes its
+// expert rows from a copy of n2 in sorted-slot order, loaded by TMA boxes, instead of gathering them
+// by token index; it writes that copy itself before its first expert item. From 1025 tokens (tiles
+// of 256) up to kPairGateUpT it stays on single SMs with gathered token rows, where the copy's cost
 // is not yet repaid. Layer time, uniform routing, single SMs vs pairs: T = 1500 372.5 vs 384.3 us,
 // 2048 402.9 vs 415.2, 2560 448.1 vs 456.0, 3072 474.8 vs 479.3, 4096 636.0 vs 621.6.
 constexpr int kPairGateUpT = 3072;
-// Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores (no fold kernel).
+// Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores, with the top-k and
+// the counting sort in the same kernel (route_small_kernel).
 constexpr int kRouterFmaT = 64;
 // Largest batch for which the down GEMM lets the combine kernel launch before it ends.
 constexpr int kEarlyCombineT = 64;
-cudaError_t launch_router_fma(const RouteParams& p, const Buffers& b, cudaStream_t s);
+cudaError_t launch_route_small(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_router_logits(const CUtensorMap& map_w, const RouteParams& p, const Buffers& b, cudaStream_t s);
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s);

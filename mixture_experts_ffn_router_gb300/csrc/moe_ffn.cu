@@ -110,7 +110,7 @@ int choose_bn(int T) {
 }
 
 struct Layout {
-  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, tile_off, n_exp_tiles, done_ctr, sched,
+  size_t logits_part, logits, topk_idx, topk_w, gap, hist, base, counts, offsets, tile_off, n_exp_tiles, done_ctr, sched, small_ctr,
       exp_tiles,
       perm, w_sorted, slot_pos, n1, n2, h, h_dense, y, d, status, wsplit, total;
   int max_tiles;
@@ -141,6 +141,7 @@ Layout make_layout(const moe_ffn_config& c) {
   L.n_exp_tiles = take(4);
   L.done_ctr = take(4);
   L.sched = take(12);
+  L.small_ctr = take(32);
   L.status = take(4);
   L.exp_tiles = take(static_cast<size_t>(L.max_tiles) * 16);
   L.perm = take(S * 4);
@@ -271,6 +272,7 @@ int moe_ffn_init(moe_ffn_ctx** out, const moe_ffn_config* cfg, void* workspace, 
   b.n_exp_tiles = reinterpret_cast<int32_t*>(w + L.n_exp_tiles);
   b.done_ctr = reinterpret_cast<int32_t*>(w + L.done_ctr);
   b.sched = reinterpret_cast<int32_t*>(w + L.sched);
+  b.small_ctr = reinterpret_cast<int32_t*>(w + L.small_ctr);
   b.status = reinterpret_cast<unsigned int*>(w + L.status);
   b.exp_tiles = reinterpret_cast<int4*>(w + L.exp_tiles);
   b.perm = reinterpret_cast<int32_t*>(w + L.perm);
@@ -529,13 +531,14 @@ static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weigh
     if (c->ev_start[k]) e = cudaEventRecord(c->ev_start[k], s);
     if (e != cudaSuccess) break;
     switch (k) {
-      // Small batches: no fold kernel, the router's sums on CUDA cores.
+      // Small batches: no fold kernel; the router's sums on CUDA cores, the top-k and the counting
+      // sort in the same kernel (slot 1), so slots 0, 2 and 3 launch nothing.
       case 0: e = T <= kRouterFmaT ? cudaSuccess : launch_router_prep(rp, c->buf, s); break;
       case 1:
-        e = T <= kRouterFmaT ? launch_router_fma(rp, c->buf, s) : launch_router_logits(c->map_wsplit, rp, c->buf, s);
+        e = T <= kRouterFmaT ? launch_route_small(rp, c->buf, s) : launch_router_logits(c->map_wsplit, rp, c->buf, s);
         break;
-      case 2: e = launch_route_topk(rp, c->buf, s); break;
-      case 3: e = launch_route_scatter(rp, c->buf, s); break;
+      case 2: e = T <= kRouterFmaT ? cudaSuccess : launch_route_topk(rp, c->buf, s); break;
+      case 3: e = T <= kRouterFmaT ? cudaSuccess : launch_route_scatter(rp, c->buf, s); break;
       case 4:
         e = cvt     ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, gemm_full, grid_gu, s)
             : pairs_gu ? launch_gate_up_pair(gu, c->buf, pin, T, gemm_full, grid_gu_launch, s)
@@ -672,7 +675,8 @@ int moe_ffn_set_kernel_events(moe_ffn_ctx* c, int kernel, void* start, void* sto
 static int slots_of(int T, int* slots) {
   if (T == 0) return 0;
   int n = 0;
-  for (int k = T > kRouterFmaT ? 0 : 1; k < kKernelsPerForward; ++k) slots[n++] = k;
+  for (int k = 0; k < kKernelsPerForward; ++k)
+    if (T > kRouterFmaT || (k != 0 && k != 2 && k != 3)) slots[n++] = k;
   return n;
 }
 

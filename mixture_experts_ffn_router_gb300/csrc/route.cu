@@ -29,17 +29,250 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 // An unsigned key with the order of the fp32 values (finite; -0 taken as +0), so that a warp
 // maximum of keys is the maximum logit.
 __device__ __forceinline__ uint32_t order_key(float v) {
   const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The fp32 value of an order key (the inverse of order_key; -0 comes back as +0).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// v[j] for a j known at run time, without local memory.
+__device__ __forceinline__ float pick4(const float (&v)[4], int j) {
+  return j == 0 ? v[0] : j == 1 ? v[1] : j == 2 ? v[2] : v[3];
+}
+
+// The routing of NT tokens by one warp, from their raw router sums. Lane l holds z[u][j], token
+// u's sum over the hidden dimension for expert l + 32 j, and inv[u], the token's 1 / RMS. Logits
+// are z * inv * router_scale (stored to rows[u] unless it is NULL); then an fp32 softmax over the
+// 128 experts; the top 8 by logit, ties to the lower expert id, and the 9th for the gap; the 8
+// probabilities renormalised to sum 1 and multiplied by per_expert_scale (pes, 128 values).
+// Lanes 0..7 get the lane-th selected expert in ascending id (e_out) and its weight (w_out); every
+// lane gets the 8th-minus-9th logit gap. The tokens' steps are interleaved for NT > 1; each
+// token's arithmetic is the same for every NT.
+template <int NT>
+__device__ __forceinline__ void route_tokens(const float (&z)[NT][4], const float (&inv)[NT], float router_scale,
+                                             float* const (&rows)[NT], const float* pes, int lane, int (&e_out)[NT],
+                                             float (&w_out)[NT], float (&gap)[NT]) {
+  constexpr unsigned kAll = 0xffffffffu;
+  float lg[NT][4], pr[NT][4], zsum[NT];
+  uint32_t mk[NT];
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      lg[u][j] = z[u][j] * inv[u] * router_scale;
+      if (rows[u]) rows[u][lane + 32 * j] = lg[u][j];
+    }
+    mk[u] = order_key(fmaxf(fmaxf(lg[u][0], lg[u][1]), fmaxf(lg[u][2], lg[u][3])));
+  }
+  // The largest logit (the warp maximum of the keys), then exp(logit - max) and their sum in a
+  // fixed butterfly order.
+#pragma unroll
+  for (int u = 0; u < NT; ++u) mk[u] = __reduce_max_sync(kAll, mk[u]);
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    const float m = key_value(mk[u]);
+    zsum[u] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pr[u][j] = expf(lg[u][j] - m);
+      zsum[u] += pr[u][j];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int u = 0; u < NT; ++u) zsum[u] += __shfl_xor_sync(kAll, zsum[u], o);
+#pragma unroll
+  for (int u = 0; u < NT; ++u)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pr[u][j] = pr[u][j] / zsum[u];
+
+  // Top-8 (and the 9th for the gap) by repeated warp arg-max. Each round: the lane's best untaken
+  // logit (the lower j, so the lower id, on equal values), the warp maximum of their keys, then the
+  // lowest expert id among the lanes holding it.
+  unsigned taken[NT];
+  int sel_e[NT][K];
+  float sel_p[NT][K];
+  float l8[NT], l9[NT];
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    taken[u] = 0u;
+    l8[u] = 0.0f;
+    l9[u] = 0.0f;
+  }
+#pragma unroll
+  for (int r = 0; r < K + 1; ++r) {
+    uint32_t key[NT];
+    int bj[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      bj[u] = -1;
+      float bl = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (!(taken[u] & (1u << j)) && (bj[u] < 0 || lg[u][j] > bl)) {
+          bj[u] = j;
+          bl = lg[u][j];
+        }
+      key[u] = bj[u] < 0 ? 0u : order_key(bl);
+    }
+    uint32_t kmax[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) kmax[u] = __reduce_max_sync(kAll, key[u]);
+    int ew[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      const uint32_t mine =
+          (bj[u] >= 0 && key[u] == kmax[u]) ? static_cast<uint32_t>(lane + 32 * bj[u]) : 0xffffffffu;
+      ew[u] = static_cast<int>(__reduce_min_sync(kAll, mine));
+    }
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      const int wlane = ew[u] & 31, wj = ew[u] >> 5;
+      const float lw = __shfl_sync(kAll, pick4(lg[u], wj), wlane);
+      const float pw = __shfl_sync(kAll, pick4(pr[u], wj), wlane);
+      if (wlane == lane) taken[u] |= 1u << wj;
+      if (r < K) {
+        sel_e[u][r] = ew[u];
+        sel_p[u][r] = pw;
+      }
+      if (r == K - 1) l8[u] = lw;
+      if (r == K) l9[u] = lw;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    // Ascending expert id (odd-even transposition sort, identical in every lane).
+#pragma unroll
+    for (int pass = 0; pass < K; ++pass) {
+#pragma unroll
+      for (int j = (pass & 1); j + 1 < K; j += 2) {
+        if (sel_e[u][j] > sel_e[u][j + 1]) {
+          const int te = sel_e[u][j];
+          sel_e[u][j] = sel_e[u][j + 1];
+          sel_e[u][j + 1] = te;
+          const float tp = sel_p[u][j];
+          sel_p[u][j] = sel_p[u][j + 1];
+          sel_p[u][j + 1] = tp;
+        }
+      }
+    }
+    float psum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < K; ++j) psum += sel_p[u][j];
+    int e = sel_e[u][0];
+    float pp = sel_p[u][0];
+#pragma unroll
+    for (int j = 1; j < K; ++j)
+      if (lane == j) {
+        e = sel_e[u][j];
+        pp = sel_p[u][j];
+      }
+    e_out[u] = e;
+    w_out[u] = lane < K ? (pp / psum) * pes[e] : 0.0f;
+    gap[u] = l8[u] - l9[u];
+  }
+}
+
+// Warp 0 of the CTA that builds a forward's schedule. From the slot counts cnt[j] of the experts
+// lane * 4 + j: the experts' first sorted positions (an exclusive scan) and, for the experts
+// [e_lo, e_hi) this forward computes, their first token tiles (tiles of bn rows). Both scans go to
+// scan_s / tscan_s [129] and to the buffers; the tile count is published (0, with a status bit, if
+// it exceeds the list) and the GEMMs' work counters are reset.
+__device__ __forceinline__ void expert_scan(const int (&cnt)[4], const RouteParams& p, const Buffers& b, int* scan_s,
+                                            int* tscan_s, int lane) {
+  int nt[4];
+  int cs = 0, ts = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int ee = lane * 4 + j;
+    nt[j] = (ee >= p.e_lo && ee < p.e_hi) ? (cnt[j] + p.bn - 1) / p.bn : 0;
+    cs += cnt[j];
+    ts += nt[j];
+  }
+  int ci = cs, ti = ts;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ci, o);
+    const int c = __shfl_up_sync(0xffffffffu, ti, o);
+    if (lane >= o) {
+      ci += a;
+      ti += c;
+    }
+  }
+  int cex = ci - cs, tex = ti - ts;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int ee = lane * 4 + j;
+    scan_s[ee] = cex;
+    tscan_s[ee] = tex;
+    b.counts[ee] = cnt[j];
+    b.offsets[ee] = cex;
+    b.tile_off[ee] = tex;
+    cex += cnt[j];
+    tex += nt[j];
+  }
+  if (lane == 31) {
+    scan_s[E] = cex;
+    tscan_s[E] = tex;
+    b.offsets[E] = cex;
+    b.tile_off[E] = tex;
+    if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
+    *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
+    b.sched[0] = 0;  // the GEMMs of this forward claim their work items from these counters
+    b.sched[1] = 0;
+    b.sched[2] = 0;  // warps done with the sorted copy of n2 (SM-pair gate_up)
+  }
+}
+
+// Expert e's token tiles (expert, first sorted row, rows, 0) from the scans above.
+__device__ __forceinline__ void expert_tiles(int e, const RouteParams& p, const Buffers& b, const int* scan_s,
+                                             const int* tscan_s) {
+  if (tscan_s[E] > b.max_tiles) return;
+  const int cnt = scan_s[e + 1] - scan_s[e];
+  const int nt = tscan_s[e + 1] - tscan_s[e];
+  for (int j = 0; j < nt; ++j) {
+    const int rows = min(p.bn, cnt - j * p.bn);
+    b.exp_tiles[tscan_s[e] + j] = make_int4(e, scan_s[e] + j * p.bn, rows, 0);
+  }
+}
+
+// One 16-byte chunk (8 features) of a pre-norm row: x * inv_rms * (1 + w), the weights given as
+// two float4 halves already holding 1 + w.
+__device__ __forceinline__ uint4 norm_chunk(uint4 xc, float inv, float4 a0, float4 a1) {
+  const float g[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
+    o[j] = pack_bf16(lo * g[2 * j], hi * g[2 * j + 1]);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 1 / RMS of one token row held by a warp (lane l: 16-byte chunks l + 32 c): lane sums in chunk
+// order, then a butterfly, so every kernel that takes it gets the same bits.
+__device__ __forceinline__ float token_inv_rms(const uint4 (&xr)[11], float eps) {
+  float ss = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 11; ++c) {
+    const uint32_t w4[4] = {xr[c].x, xr[c].y, xr[c].z, xr[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(w4[j]), bb = bf16_hi(w4[j]);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(bb, bb, ss);
+    }
+  }
+  ss = warp_sum(ss);
+  return 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -88,34 +321,22 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     const int t = blockIdx.x * tb + warp * p.tpw + i;
     if (t >= p.T) break;
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
-    float ss = 0.0f;
+    float inv;
     {
       uint4 xv[11];
 #pragma unroll
       for (int c = 0; c < 11; ++c) xv[c] = __ldg(xr + lane + 32 * c);
-#pragma unroll
-      for (int c = 0; c < 11; ++c) {
-        const uint32_t w4[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float a = bf16_lo(w4[j]), bb = bf16_hi(w4[j]);
-          ss = fmaf(a, a, ss);
-          ss = fmaf(bb, bb, ss);
-        }
-      }
+      inv = token_inv_rms(xv, p.eps);
     }
-    ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + p.eps);
 
     if (lane == 0) inv_s[warp * p.tpw + i] = inv;
 
     // Logits: expert e = lane + 32 j. The partial sums of the lane's 4 experts are added in
     // ascending split order, loaded 8 splits (32 loads) at a time, the last group predicated.
-    float lg[4], pr[4];
+    float z[1][4] = {{0.0f, 0.0f, 0.0f, 0.0f}};
     {
       const float* pp = b.logits_part + static_cast<size_t>(t) * E + lane;
       const size_t stride = static_cast<size_t>(p.T) * E;
-      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       for (int s = 0; s < p.ks; s += 8) {
         float a[8][4];
 #pragma unroll
@@ -126,90 +347,20 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
         for (int u = 0; u < 8; ++u)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (s + u < p.ks) z[j] += a[u][j];
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        lg[j] = z[j] * inv * p.router_scale;
-        b.logits[static_cast<size_t>(t) * E + lane + 32 * j] = lg[j];
+            if (s + u < p.ks) z[0][j] += a[u][j];
       }
     }
-    const float m = warp_max(fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3])));
-    float zsum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      pr[j] = expf(lg[j] - m);
-      zsum += pr[j];
-    }
-    zsum = warp_sum(zsum);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) pr[j] = pr[j] / zsum;
-
-    // Top-8 (and the 9th for the gap) by repeated warp arg-max.
-    unsigned taken = 0;
-    int sel_e[K];
-    float sel_p[K];
-    float l8 = 0.0f, l9 = 0.0f;
-    // Each round: the lane's best untaken logit (the lower j, so the lower id, on equal values),
-    // the warp maximum of their keys, then the lowest expert id among the lanes holding it.
-#pragma unroll
-    for (int r = 0; r < K + 1; ++r) {
-      int bj = -1;
-      float bl = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (!(taken & (1u << j)) && (bj < 0 || lg[j] > bl)) {
-          bj = j;
-          bl = lg[j];
-        }
-      const uint32_t key = bj < 0 ? 0u : order_key(bl);
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const uint32_t mine = (bj >= 0 && key == kmax) ? static_cast<uint32_t>(lane + 32 * bj) : 0xffffffffu;
-      const int ew = static_cast<int>(__reduce_min_sync(0xffffffffu, mine));
-      const int wlane = ew & 31, wj = ew >> 5;
-      const float lw = __shfl_sync(0xffffffffu, wj == 0 ? lg[0] : wj == 1 ? lg[1] : wj == 2 ? lg[2] : lg[3], wlane);
-      const float pw = __shfl_sync(0xffffffffu, wj == 0 ? pr[0] : wj == 1 ? pr[1] : wj == 2 ? pr[2] : pr[3], wlane);
-      if (wlane == lane) taken |= 1u << wj;
-      if (r < K) {
-        sel_e[r] = ew;
-        sel_p[r] = pw;
-      }
-      if (r == K - 1) l8 = lw;
-      if (r == K) l9 = lw;
-    }
-    // Ascending expert id (odd-even transposition sort, identical in every lane).
-#pragma unroll
-    for (int pass = 0; pass < K; ++pass) {
-#pragma unroll
-      for (int j = (pass & 1); j + 1 < K; j += 2) {
-        if (sel_e[j] > sel_e[j + 1]) {
-          const int te = sel_e[j];
-          sel_e[j] = sel_e[j + 1];
-          sel_e[j + 1] = te;
-          const float tp = sel_p[j];
-          sel_p[j] = sel_p[j + 1];
-          sel_p[j + 1] = tp;
-        }
-      }
-    }
-    float psum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < K; ++j) psum += sel_p[j];
+    const float invs[1] = {inv};
+    float* const rows[1] = {b.logits + static_cast<size_t>(t) * E};
+    int sel[1];
+    float wsel[1], gap[1];
+    route_tokens<1>(z, invs, p.router_scale, rows, pes_s, lane, sel, wsel, gap);
     if (lane < K) {
-      int e = sel_e[0];
-      float pp = sel_p[0];
-#pragma unroll
-      for (int j = 1; j < K; ++j)
-        if (lane == j) {
-          e = sel_e[j];
-          pp = sel_p[j];
-        }
-      const float w = (pp / psum) * pes_s[e];
-      b.topk_idx[static_cast<size_t>(t) * K + lane] = e;
-      b.topk_w[static_cast<size_t>(t) * K + lane] = w;
-      atomicAdd(&hist_s[e], 1);
+      b.topk_idx[static_cast<size_t>(t) * K + lane] = sel[0];
+      b.topk_w[static_cast<size_t>(t) * K + lane] = wsel[0];
+      atomicAdd(&hist_s[sel[0]], 1);
     }
-    if (lane == 0) b.gap[t] = l8 - l9;
+    if (lane == 0) b.gap[t] = gap[0];
   }
 
   // Per-CTA counts, then the last CTA to arrive builds the offsets, bases and tile list.
@@ -253,51 +404,12 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     }
     __syncthreads();
     if (warp == 0) {
-      // Exclusive scans over the 128 experts of the counts and of the token-tile counts.
-      int cnt[4], nt[4];
-      int cs = 0, ts = 0;
+      // Exclusive scans over the 128 experts of the counts and of the token-tile counts (tiles only
+      // for the experts this forward computes: all of them, or a shard's range).
+      int cnt[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ee = lane * 4 + j;
-        cnt[j] = part_s[0][ee] + part_s[1][ee];
-        // Token tiles only for the experts this forward computes (all of them, or a shard's range).
-        nt[j] = (ee >= p.e_lo && ee < p.e_hi) ? (cnt[j] + p.bn - 1) / p.bn : 0;
-        cs += cnt[j];
-        ts += nt[j];
-      }
-      int ci = cs, ti = ts;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, ci, o);
-        const int c = __shfl_up_sync(0xffffffffu, ti, o);
-        if (lane >= o) {
-          ci += a;
-          ti += c;
-        }
-      }
-      int cex = ci - cs, tex = ti - ts;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ee = lane * 4 + j;
-        scan_s[ee] = cex;
-        tscan_s[ee] = tex;
-        b.counts[ee] = cnt[j];
-        b.offsets[ee] = cex;
-        b.tile_off[ee] = tex;
-        cex += cnt[j];
-        tex += nt[j];
-      }
-      if (lane == 31) {
-        scan_s[E] = cex;
-        tscan_s[E] = tex;
-        b.offsets[E] = cex;
-        b.tile_off[E] = tex;
-        if (tex > b.max_tiles) atomicOr(b.status, kStatusBadSchedule);
-        *b.n_exp_tiles = tex <= b.max_tiles ? tex : 0;
-        b.sched[0] = 0;  // the GEMMs of this forward claim their work items from these counters
-        b.sched[1] = 0;
-        b.sched[2] = 0;  // warps done with the sorted copy of n2 (SM-pair gate_up)
-      }
+      for (int j = 0; j < 4; ++j) cnt[j] = part_s[0][lane * 4 + j] + part_s[1][lane * 4 + j];
+      expert_scan(cnt, p, b, scan_s, tscan_s, lane);
     }
     __syncthreads();
     {
@@ -321,14 +433,7 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
           }
       }
     }
-    if (half == 0 && tscan_s[E] <= b.max_tiles) {
-      const int cnt = scan_s[e + 1] - scan_s[e];
-      const int nt = tscan_s[e + 1] - tscan_s[e];
-      for (int j = 0; j < nt; ++j) {
-        const int rows = min(p.bn, cnt - j * p.bn);
-        b.exp_tiles[tscan_s[e] + j] = make_int4(e, scan_s[e] + j * p.bn, rows, 0);
-      }
-    }
+    if (half == 0) expert_tiles(e, p, b, scan_s, tscan_s);
   }
 
   // The normalised rows are written only now: the routing above never waits behind these stores
@@ -339,52 +444,255 @@ __global__ void __launch_bounds__(256, 4) route_topk_kernel(RouteParams p, Buffe
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
     const float inv = inv_s[warp * p.tpw + i];
     // Expert-branch input n2 and dense-branch input n1 (n2 only where the gate_up GEMM gathers
-    // its rows by token index; above kPermRowsT tokens the gate_up GEMM writes them itself, in
-    // sorted-slot order).
+    // its rows by token index; above kPairGateUpT tokens the SM-pair gate_up GEMM writes them itself,
+    // in sorted-slot order).
     uint4* n2r = reinterpret_cast<uint4*>(b.n2 + static_cast<size_t>(t) * H);
-    if (p.full_layer && !p.write_n2) {
+    if (p.full_layer) {
       uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
 #pragma unroll
       for (int c = 0; c < 11; ++c) {
-        const float4 a0 = g_s[0][c][0][lane], a1 = g_s[0][c][1][lane];
-        const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint4 xc = __ldg(xr + lane + 32 * c);
-        const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
-        uint32_t o1[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
-          o1[j] = pack_bf16(lo * g1[2 * j], hi * g1[2 * j + 1]);
-        }
-        n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-      }
-    } else if (p.full_layer) {
-      uint4* n1r = reinterpret_cast<uint4*>(b.n1 + static_cast<size_t>(t) * H);
-#pragma unroll
-      for (int c = 0; c < 11; ++c) {
-        const float4 a0 = g_s[0][c][0][lane], a1 = g_s[0][c][1][lane];
-        const float4 c0 = g_s[1][c][0][lane], c1 = g_s[1][c][1][lane];
-        const float g1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float g2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         // x again, read-only (this warp read the row above), so the row does not stay in
         // registers; the weights come from shared memory, so no load waits for a store.
         const uint4 xc = __ldg(xr + lane + 32 * c);
-        const uint32_t w4[4] = {xc.x, xc.y, xc.z, xc.w};
-        uint32_t o1[4], o2[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = bf16_lo(w4[j]) * inv, hi = bf16_hi(w4[j]) * inv;
-          o1[j] = pack_bf16(lo * g1[2 * j], hi * g1[2 * j + 1]);
-          o2[j] = pack_bf16(lo * g2[2 * j], hi * g2[2 * j + 1]);
-        }
-        n1r[lane + 32 * c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-        n2r[lane + 32 * c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        n1r[lane + 32 * c] = norm_chunk(xc, inv, g_s[0][c][0][lane], g_s[0][c][1][lane]);
+        if (p.write_n2) n2r[lane + 32 * c] = norm_chunk(xc, inv, g_s[1][c][0][lane], g_s[1][c][1][lane]);
       }
     } else if (p.write_n2) {
 #pragma unroll
       for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = __ldg(xr + lane + 32 * c);
     }
   }
+}
+
+// One pre-norm row of token t, written by one warp: n1 (which = 0) or n2 (which = 1) in the full
+// layer; in the experts-only mode n2 = x (which = 0) and nothing for which = 1.
+__device__ __forceinline__ void write_norm_row(const RouteParams& p, const Buffers& b, int t, int which, int lane) {
+  const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
+  if (!p.full_layer) {
+    if (which == 0 && p.write_n2) {
+      uint4* n2r = reinterpret_cast<uint4*>(b.n2 + static_cast<size_t>(t) * H);
+#pragma unroll
+      for (int c = 0; c < 11; ++c) n2r[lane + 32 * c] = __ldg(xr + lane + 32 * c);
+    }
+    return;
+  }
+  if (which == 1 && !p.write_n2) return;
+  const float4* wr = reinterpret_cast<const float4*>(which ? p.pre_ff_ln_2 : p.pre_ff_ln);
+  uint4 xv[11];
+  float4 w[11][2];
+#pragma unroll
+  for (int c = 0; c < 11; ++c) {
+    xv[c] = __ldg(xr + lane + 32 * c);
+    w[c][0] = __ldg(wr + 2 * (lane + 32 * c));
+    w[c][1] = __ldg(wr + 2 * (lane + 32 * c) + 1);
+  }
+  const float inv = token_inv_rms(xv, p.eps);
+  uint4* out = reinterpret_cast<uint4*>((which ? b.n2 : b.n1) + static_cast<size_t>(t) * H);
+#pragma unroll
+  for (int c = 0; c < 11; ++c) {
+    const float4 a0 = w[c][0], a1 = w[c][1];
+    out[lane + 32 * c] = norm_chunk(xv[c], inv, make_float4(1.0f + a0.x, 1.0f + a0.y, 1.0f + a0.z, 1.0f + a0.w),
+                                    make_float4(1.0f + a1.x, 1.0f + a1.y, 1.0f + a1.z, 1.0f + a1.w));
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Small batches (T <= kRouterFmaT): the routing front end in one kernel, three phases chained by
+// tickets rather than by kernel boundaries.
+//   1. CTA (x, g) forms W'[e] = W_r[e] * (1 + router_norm_w) in fp32 for the four experts
+//      e = 4x .. 4x + 3 and the raw router sums of tokens 16g .. 16g + 15, two per warp, both rows
+//      loaded before any sum starts. Lane l sums h = 8 (l + 32 k) .. + 7 for k = 0..10 in that
+//      order and a butterfly adds the 32 lane sums, so every sum has one fixed order. Each CTA
+//      then draws a ticket of its token group. The group's 32 pre-norm rows (n1 and n2 of 16
+//      tokens) are written by the 31 CTAs that are not last, one row per ticket (two for the
+//      ticket before the last): one row per CTA keeps the stores coalesced and spread over SMs.
+//   2. The last CTA of the group routes its 16 tokens, two per warp (route_tokens on the sums,
+//      with the RMS each warp took from its rows in phase 1), and writes the routing results.
+//   3. The last group to finish phase 2 lists the slots by expert. A stable counting sort: the
+//      rank of token t within expert e is the number of tokens below t that chose e, counted from
+//      a 64-bit token mask per expert; then the expert offsets and the token-tile list.
+// A ticket counter is reset by the CTA that draws its last ticket, so every counter is zero again
+// when the kernel ends (the context starts them at zero).
+constexpr int kSmallTok = 16;  // tokens per CTA: two per warp
+constexpr int kSmallExp = 4;   // experts per CTA
+constexpr int kSmallFinal = 4; // small_ctr index of the phase-3 ticket (0..3: token groups)
+static_assert(kRouterFmaT <= 64 && kRouterFmaT <= 4 * kSmallTok, "token masks and group tickets");
+static_assert(E / kSmallExp == 2 * kSmallTok, "one row job (n1 or n2 of a token) per CTA of a group");
+
+__global__ void __launch_bounds__(256) route_small_kernel(RouteParams p, Buffers b) {
+  // W' of expert ee, column group q (8 columns) as two float4 halves at wp[ee][half][q], so that
+  // lanes reading groups q = lane + 32 k hit consecutive 16-byte words. Phase 3 reuses the space
+  // for the experts' token masks.
+  __shared__ float4 wp[kSmallExp][2][H / 8];
+  __shared__ int ticket_s;
+  __shared__ float pes_s[E];
+  __shared__ int scan_s[E + 1];
+  __shared__ int tscan_s[E + 1];
+  __shared__ int role_s;
+  unsigned long long* mask_s = reinterpret_cast<unsigned long long*>(&wp[0][0][0]);  // [128], phase 3
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int e0 = blockIdx.x * kSmallExp, g = blockIdx.y;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t0 = g * kSmallTok + 2 * warp;
+  const int nt = t0 >= p.T ? 0 : (t0 + 1 < p.T ? 2 : 1);
+  // The token rows first (their latency overlaps the fold), then W' of the CTA's experts and
+  // per_expert_scale.
+  uint4 xv[2][11];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(u < nt ? t0 + u : 0) * H);
+#pragma unroll
+    for (int k = 0; k < 11; ++k) xv[u][k] = u < nt ? xr[lane + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  {
+    const float4* gr = reinterpret_cast<const float4*>(p.router_norm_w);
+    for (int i = tid; i < H / 4; i += 256) {
+      const float4 gv = gr[i];
+#pragma unroll
+      for (int ee = 0; ee < kSmallExp; ++ee) {
+        const float4 w = reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e0 + ee) * H)[i];
+        wp[ee][i & 1][i >> 1] =
+            make_float4(w.x * (1.0f + gv.x), w.y * (1.0f + gv.y), w.z * (1.0f + gv.z), w.w * (1.0f + gv.w));
+      }
+    }
+  }
+  if (tid < E) pes_s[tid] = p.per_expert_scale[tid];
+  __syncthreads();
+  {
+    float acc[2][kSmallExp];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int ee = 0; ee < kSmallExp; ++ee) acc[u][ee] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+#pragma unroll
+      for (int ee = 0; ee < kSmallExp; ++ee) {
+        const float4 w0 = wp[ee][0][lane + 32 * k], w1 = wp[ee][1][lane + 32 * k];
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t x4[4] = {xv[u][k].x, xv[u][k].y, xv[u][k].z, xv[u][k].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[u][ee] = fmaf(bf16_lo(x4[j]), wv[2 * j], acc[u][ee]);
+            acc[u][ee] = fmaf(bf16_hi(x4[j]), wv[2 * j + 1], acc[u][ee]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int ee = 0; ee < kSmallExp; ++ee) {
+        acc[u][ee] = warp_sum(acc[u][ee]);
+        if (lane == u * kSmallExp + ee && u < nt) b.logits_part[static_cast<size_t>(t0 + u) * E + e0 + ee] = acc[u][ee];
+      }
+  }
+  // Ticket of the token group: its last CTA goes on to phase 2.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int ticket = atomicAdd(b.small_ctr + g, 1);
+    ticket_s = ticket;
+    role_s = ticket == static_cast<int>(gridDim.x) - 1;
+    if (role_s) b.small_ctr[g] = 0;  // every CTA of the group has drawn its ticket
+  }
+  // 1 / RMS of the two tokens (phase 2 takes it from here).
+  float inv[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) inv[u] = token_inv_rms(xv[u], p.eps);
+  __syncthreads();
+  if (!role_s) {
+    // Row jobs: job j is row j & 1 (n1, n2) of token 16 g + j / 2; ticket k takes job k, and the
+    // ticket before the last also job 31.
+    const int ticket = ticket_s;
+    const int job = warp == 0 ? ticket : (warp == 1 && ticket == static_cast<int>(gridDim.x) - 2) ? ticket + 1 : -1;
+    if (job >= 0) {
+      const int t = g * kSmallTok + (job >> 1);
+      if (t < p.T) write_norm_row(p, b, t, job & 1, lane);
+    }
+    return;
+  }
+  __threadfence();
+
+  // Phase 2: the group's sums (stored by 32 CTAs: L2-coherent loads), the routing.
+  {
+    float z[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        z[u][j] = u < nt ? 0.0f + __ldcg(b.logits_part + static_cast<size_t>(t0 + u) * E + lane + 32 * j) : 0.0f;
+    float* const rows[2] = {nt > 0 ? b.logits + static_cast<size_t>(t0) * E : nullptr,
+                            nt > 1 ? b.logits + static_cast<size_t>(t0 + 1) * E : nullptr};
+    int sel[2];
+    float wsel[2], gap[2];
+    route_tokens<2>(z, inv, p.router_scale, rows, pes_s, lane, sel, wsel, gap);
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (u < nt) {
+        if (lane < K) {
+          b.topk_idx[static_cast<size_t>(t0 + u) * K + lane] = sel[u];
+          b.topk_w[static_cast<size_t>(t0 + u) * K + lane] = wsel[u];
+        }
+        if (lane == 0) b.gap[t0 + u] = gap[u];
+      }
+  }
+  // Ticket of phase 3.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int ticket = atomicAdd(b.small_ctr + kSmallFinal, 1);
+    role_s = ticket == static_cast<int>(gridDim.y) - 1;
+    if (role_s) b.small_ctr[kSmallFinal] = 0;
+  }
+  __syncthreads();
+  if (!role_s) return;
+  __threadfence();
+
+  // Phase 3: slot s = 8 t + k, two per thread (S <= 512).
+  if (tid < E) mask_s[tid] = 0ull;
+  __syncthreads();
+  const int S = p.T * K;
+  int se[2];
+  float sw[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int sl = tid + 256 * i;
+    se[i] = -1;
+    sw[i] = 0.0f;
+    if (sl < S) {
+      se[i] = __ldcg(b.topk_idx + sl);
+      sw[i] = __ldcg(b.topk_w + sl);
+      if (se[i] < 0 || se[i] >= E) {
+        atomicOr(b.status, kStatusBadIndex);
+        se[i] = -1;
+      } else {
+        atomicOr(&mask_s[se[i]], 1ull << (sl >> 3));
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int cnt[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cnt[j] = __popcll(mask_s[lane * 4 + j]);
+    expert_scan(cnt, p, b, scan_s, tscan_s, lane);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int sl = tid + 256 * i;
+    if (se[i] < 0) continue;
+    const int t = sl >> 3;
+    const int pos = scan_s[se[i]] + __popcll(mask_s[se[i]] & ((1ull << t) - 1ull));
+    b.perm[pos] = t;
+    b.w_sorted[pos] = sw[i];
+    b.slot_pos[sl] = pos;
+  }
+  if (tid < E) expert_tiles(tid, p, b, scan_s, tscan_s);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -646,6 +954,11 @@ cudaError_t launch_finish(const CombineParams& p, const float* moe_sum, const fl
 cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream_t s) {
   const int tb = 8 * p.tpw;
   return launch_pdl(route_topk_kernel, dim3((p.T + tb - 1) / tb), dim3(256), 0, s, p, b);
+}
+
+cudaError_t launch_route_small(const RouteParams& p, const Buffers& b, cudaStream_t s) {
+  if (p.T < 1 || p.T > kRouterFmaT) return cudaErrorInvalidValue;
+  return launch_pdl(route_small_kernel, dim3(E / kSmallExp, (p.T + kSmallTok - 1) / kSmallTok), dim3(256), 0, s, p, b);
 }
 
 cudaError_t launch_route_scatter(const RouteParams& p, const Buffers& b, cudaStream_t s) {

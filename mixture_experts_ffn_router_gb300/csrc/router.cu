@@ -284,89 +284,6 @@ cudaError_t router_set_smem_limit() {
                               RCfg<kRouterSmallN>::kSmem);
 }
 
-// Small batches (T <= kRouterFmaT): the same sums on CUDA cores in fp32, no fold kernel before
-// them. CTA (x, g) forms W'[e] = W_r[e] * (1 + router_norm_w) in fp32 in shared memory for the four
-// experts e = 4 x .. 4 x + 3 (the fold the tensor-core path splits into bf16 parts) and takes tokens
-// 16 g .. 16 g + 15, two per warp, both rows loaded before any sum starts. Lane l sums
-// h = 8 (l + 32 k) .. + 7 for k = 0..10 in that order and a butterfly adds the 32 lane sums, so
-// every sum has one fixed order. One partial per token (ks = 1).
-constexpr int kRouterFmaThreads = 256;
-constexpr int kRouterFmaTok = 16;  // tokens per CTA: two per warp
-constexpr int kRouterFmaExp = 4;   // experts per CTA
-
-__global__ void __launch_bounds__(kRouterFmaThreads) router_fma_kernel(RouteParams p, Buffers b) {
-  // W' of expert ee, column group q (8 columns) as two float4 halves at wp[ee][half][q], so that
-  // lanes reading groups q = lane + 32 k hit consecutive 16-byte words (no bank conflicts).
-  __shared__ float4 wp[kRouterFmaExp][2][H / 8];
-  const int e0 = blockIdx.x * kRouterFmaExp;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_launch_dependents();
-  // As in the tensor-core path: the top-k kernel's finish counter and its per-chunk expert
-  // counts start every forward from zero.
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *b.done_ctr = 0;
-  if (blockIdx.y == 0 && threadIdx.x < E)
-    for (int c = blockIdx.x; c < (p.T + kScatterTok - 1) / kScatterTok; c += gridDim.x)
-      b.hist[c * E + threadIdx.x] = 0;
-  const int t0 = blockIdx.y * kRouterFmaTok + 2 * warp;
-  const int nt = t0 >= p.T ? 0 : (t0 + 1 < p.T ? 2 : 1);
-  // The token rows first (their latency overlaps the fold), then W' of the CTA's experts.
-  uint4 xv[2][11];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(u < nt ? t0 + u : 0) * H);
-#pragma unroll
-    for (int k = 0; k < 11; ++k) xv[u][k] = u < nt ? xr[lane + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
-  }
-  const float4* gr = reinterpret_cast<const float4*>(p.router_norm_w);
-  for (int i = threadIdx.x; i < H / 4; i += kRouterFmaThreads) {
-    const float4 g = gr[i];
-#pragma unroll
-    for (int ee = 0; ee < kRouterFmaExp; ++ee) {
-      const float4 w = reinterpret_cast<const float4*>(p.router_w + static_cast<size_t>(e0 + ee) * H)[i];
-      wp[ee][i & 1][i >> 1] = make_float4(w.x * (1.0f + g.x), w.y * (1.0f + g.y), w.z * (1.0f + g.z), w.w * (1.0f + g.w));
-    }
-  }
-  __syncthreads();
-  float acc[2][kRouterFmaExp];
-#pragma unroll
-  for (int u = 0; u < 2; ++u)
-#pragma unroll
-    for (int ee = 0; ee < kRouterFmaExp; ++ee) acc[u][ee] = 0.0f;
-#pragma unroll
-  for (int k = 0; k < 11; ++k) {
-#pragma unroll
-    for (int ee = 0; ee < kRouterFmaExp; ++ee) {
-      const float4 w0 = wp[ee][0][lane + 32 * k], w1 = wp[ee][1][lane + 32 * k];
-      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t x4[4] = {xv[u][k].x, xv[u][k].y, xv[u][k].z, xv[u][k].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[u][ee] = fmaf(__uint_as_float(x4[j] << 16), wv[2 * j], acc[u][ee]);
-          acc[u][ee] = fmaf(__uint_as_float(x4[j] & 0xFFFF0000u), wv[2 * j + 1], acc[u][ee]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < 2; ++u)
-#pragma unroll
-    for (int ee = 0; ee < kRouterFmaExp; ++ee) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[u][ee] += __shfl_xor_sync(0xffffffffu, acc[u][ee], o);
-      if (lane == u * kRouterFmaExp + ee && u < nt) b.logits_part[static_cast<size_t>(t0 + u) * E + e0 + ee] = acc[u][ee];
-    }
-}
-
-cudaError_t launch_router_fma(const RouteParams& p, const Buffers& b, cudaStream_t s) {
-  if (p.T > kRouterFmaT || p.ks != 1) return cudaErrorInvalidValue;
-  return launch_pdl(router_fma_kernel, dim3(E / kRouterFmaExp, (p.T + kRouterFmaTok - 1) / kRouterFmaTok),
-                    dim3(kRouterFmaThreads), 0,
-                    s, p, b);
-}
-
 cudaError_t launch_router_prep(const RouteParams& p, const Buffers& b, cudaStream_t s) {
   return launch_pdl(router_prep_kernel, dim3(E), dim3(kPrepThreads), 0, s, p, b);
 }

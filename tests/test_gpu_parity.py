@@ -42,9 +42,22 @@ def test_moe_only_small(T):
     _full_check(MOE, T, 100 + T, label="moe-only T=%d" % T)
 
 
-@pytest.mark.parametrize("T", [64, 1, 16, 65, 200])
+@pytest.mark.parametrize("T", [64, 1, 16, 17, 50, 65, 200])
 def test_full_layer(T):
+    # Up to 64 tokens the routing front end is one kernel in token groups of 16 (17 and 50 end in
+    # a partly filled group); from 65 the router, top-k and scatter kernels run apart.
     _full_check(FULL, T, 200 + T, label="full T=%d" % T)
+
+
+def test_kernel_slots_by_batch_size():
+    m = B.MoeFFN(FULL, 256)
+    for T in (1, 17, 64):
+        assert B.moe_ffn_kernel_slots(m.ctx, T) == [1, 4, 5, 6]
+        assert [B.slot_name(k, T) for k in (1, 4)] == ["route_small", "gate_up_gemm"]
+    for T in (65, 256):
+        assert B.moe_ffn_kernel_slots(m.ctx, T) == [0, 1, 2, 3, 4, 5, 6]
+        assert B.slot_name(1, T) == "router_logits"
+    assert B.moe_ffn_kernel_slots(m.ctx, 0) == []
 
 
 def _sampled_check(mode, T, seed, skew, n_sample, label):
