@@ -93,6 +93,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true",
                    help="default workload only: skip the T=4096 prefill leg of the line")
+    p.add_argument("--no-configs", action="store_true",
+                   help="default workload only: skip the other configurations (experts-only T=8, the T sweep, "
+                        "the 30-layer stack) measured after the two legs of the line")
     p.add_argument("--ep", action="store_true",
                    help="expert parallel: each rank runs its contiguous share of the 128 experts on the same "
                         "tokens, then the partial expert sums are all-reduced (NCCL) before the post norms")
@@ -660,6 +663,50 @@ def run_ep(args, wl):
     return 0
 
 
+SWEEP_T = (1, 16, 256, 1024, 4096, 16384)
+
+
+def compact_result(res, wl, args):
+    """The figures of one measured configuration, for the line's `configs` object."""
+    lr, rf, ck = res["layer_roofline"], res["roofline"], res["clocks"] or {}
+    return {"workload": wl["desc"], "T": wl["T"], "value": res["value"], "unit": UNIT,
+            "ms_per_step": res["ms_per_step"], "steps": args.steps, "warmup": max(args.warmup, 3),
+            "layer_roofline": {k: lr[k] for k in ("frac", "bound", "roofline_us", "step_us", "experts_hit")},
+            "roofline": {k: rf[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac", "traffic")},
+            "e2e": res["e2e"]["value"], "gpu_launches": res["gpu_launches"],
+            "clocks": {k: ck.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "in_timed_region")},
+            "kernels_us": res["kernels_us"]}
+
+
+def run_configs(args, layer_weights, dev, world, rank, clocks):
+    import torch
+    from mixture_experts_ffn_router_gb300 import synth
+
+    out = {}
+    wl = dict(WORKLOADS["moe8"])
+    w_moe = synth.make_weights(seed=args.seed, layer=0, device=dev, full_layer=False, skew=False)
+    x = synth.make_x(wl["T"], seed=args.seed, device=dev)
+    out["moe8"] = compact_result(measure(args, wl, [w_moe], x, dev, world, rank, False, clocks, "moe8"), wl, args)
+    del w_moe
+    sweep = {"T=64": "the line's value (decode64)"}
+    for T in SWEEP_T:
+        wl = workload_of(argparse.Namespace(workload="layer", T=T))
+        x = synth.make_x(T, seed=args.seed, device=dev)
+        sweep["T=%d" % T] = compact_result(measure(args, wl, [layer_weights], x, dev, world, rank, False, clocks,
+                                                   "layer"), wl, args)
+    out["sweep"] = sweep
+    wl = dict(WORKLOADS["stack30"])
+    ws = [synth.make_weights(seed=args.seed, layer=l, device=dev, full_layer=True, skew=False)
+          for l in range(wl["layers"])]
+    x = synth.make_x(wl["T"], seed=args.seed, device=dev)
+    res = measure(args, wl, ws, x, dev, world, rank, False, clocks, "stack30")
+    out["stack30"] = {**compact_result(res, wl, args), "layers": wl["layers"],
+                      "note": "value is end-to-end tokens/s through all 30 layers; layer_roofline is per layer"}
+    del ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl):
     import torch
     from mixture_experts_ffn_router_gb300 import synth
@@ -704,6 +751,13 @@ def run_ours(args, wl):
         prefill = {"metric": METRIC, "unit": UNIT, "steps": args.steps, "warmup": max(args.warmup, 3),
                    "config": config_of(wl_p, world), **prefill}
         del prefill["cpu_baseline"]
+    # The block's other configurations, measured in the same process under the same rules, so that
+    # every configuration the metric is reported on has a number from this run: the experts-only
+    # block at T=8, the full layer swept over T with uniform routing (T=64 is the line's value),
+    # and the 30-layer stack at T=256.
+    configs = None
+    if args.workload == "decode64" and not args.no_configs:
+        configs = run_configs(args, weights[0], dev, world, rank, clocks)
     time.sleep(0.25)
     clocks.stop()
 
@@ -720,6 +774,8 @@ def run_ours(args, wl):
         }
         if prefill is not None:
             line["prefill4096"] = prefill
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -232,11 +232,12 @@ int moe_ffn_device_status(moe_ffn_ctx* ctx, void* stream, uint32_t* word);
  * right before the launch of kernel slot `kernel` and `stop` right after it. NULL events turn the
  * hook off. Slots (0..6): 0 router matrix split, 1 router logits, 2 top-k and pre-norms,
  * 3 permutation (counting-sort scatter), 4 gate_up grouped GEMM, 5 down grouped GEMM, 6 combine and
- * post-norms. Forwards of at most 64 tokens launch nothing at slot 0 (their router sums run on CUDA
- * cores in slot 1), so its two events are recorded back to back (moe_ffn_kernel_slots). */
+ * post-norms. Forwards of at most 64 tokens run the whole routing front end (router sums on CUDA
+ * cores, top-k, pre-norms, counting sort) as one kernel in slot 1 and launch nothing at slots 0, 2
+ * and 3, whose events are then recorded back to back (moe_ffn_kernel_slots). */
 int moe_ffn_set_kernel_events(moe_ffn_ctx* ctx, int kernel, void* start, void* stop);
 
-/* Number of kernels one forward of T tokens launches on the device (0 for T = 0; 6 for T <= 64,
+/* Number of kernels one forward of T tokens launches on the device (0 for T = 0; 4 for T <= 64,
  * else 7). */
 int moe_ffn_kernels_per_forward(const moe_ffn_ctx* ctx, int T);
 

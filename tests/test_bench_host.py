@@ -95,3 +95,24 @@ def test_clock_summary_names_its_window():
     assert not after["in_timed_region"] and after["samples"] == 1 and "right after" in after["window"]
     none = c.summary(10.6, 10.61)
     assert none["samples"] == 0 and not none["in_timed_region"]
+
+
+def test_default_run_covers_every_configuration():
+    # Beside the decode value and the prefill leg, the default run measures the experts-only block
+    # at T=8, the sweep's other sizes and the 30-layer stack, so each configuration the metric is
+    # reported on gets a number from the same run.
+    a = bench.parse_args([])
+    assert not a.no_configs
+    assert set(bench.SWEEP_T) | {64} == {1, 16, 64, 256, 1024, 4096, 16384}
+    assert bench.WORKLOADS["moe8"]["T"] == 8 and not bench.WORKLOADS["moe8"]["full"]
+    assert bench.WORKLOADS["stack30"]["layers"] == 30 and bench.WORKLOADS["stack30"]["T"] == 256
+    res = {"value": 1.0, "ms_per_step": 0.5,
+           "layer_roofline": {"frac": 0.9, "bound": "hbm", "roofline_us": 200.0, "step_us": 222.0, "experts_hit": 8,
+                              "bytes": 1, "flops": 2},
+           "roofline": {"kernel": "gate_up_gemm", "bound": "hbm", "achieved": 6000.0, "peak": 6794.5,
+                        "unit": "GB/s", "frac": 0.88, "traffic": None, "kernel_us": 1.0},
+           "e2e": {"value": 0.9}, "gpu_launches": 80, "clocks": {"sm_mhz": 2070.0, "reasons": []},
+           "kernels_us": {"combine": 1.0}}
+    c = bench.compact_result(res, bench.WORKLOADS["moe8"], a)
+    assert c["T"] == 8 and c["value"] == 1.0 and c["warmup"] >= 3 and c["e2e"] == 0.9
+    assert c["layer_roofline"]["frac"] == 0.9 and c["roofline"]["kernel"] == "gate_up_gemm"
