@@ -304,6 +304,60 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // The down GEMM's tile list was written two kernels back, by a kernel that had completed before
+  // gate_up passed its own dependency wait and let this grid launch, and its weights are inputs.
+  // So its producer claims its first item and issues that item's first weight stages before the
+  // wait, while gate_up's last items still run; the token rows (gate_up's output) follow after it.
+  // Token tiles of at most 64 only: at T = 64 the forward ends 1.1 us earlier (the first weight
+  // load moves from 1.6 us after gate_up's end to 11 us before it), at T = 1 1.7 us earlier; with
+  // tiles of 128 (T = 1024) the down GEMM ended 6 us later.
+  constexpr bool kPreload = !GATE_UP && !CVT && BN <= 64;
+  // Each role decodes items with a binary search over the experts' first tiles; keep them on chip.
+  __shared__ int tile_off_s[E + 1];
+  int n_tiles = 0;
+  auto load_tiles = [&]() {
+    n_tiles = *reinterpret_cast<volatile int*>(b.n_exp_tiles);
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) tile_off_s[e] = b.tile_off[e];
+    __syncthreads();
+  };
+  if (kPreload) load_tiles();
+  const int n_dense_tiles = full_layer ? (T + BN - 1) / BN : 0;
+  const int n_dense_items = n_dense_tiles * C::kMtDense;
+  // The producer's item claimed before the wait (-2: none) and its stages armed there.
+  int pre_item = -2, pre_stages = 0;
+  if (kPreload && warp == 0) {
+    if (lane == 0) {
+      const int total0 = n_dense_items + n_tiles * C::kMtExp;
+      const int i0 = atomicAdd(b.sched + 1, 1);
+      pre_item = i0 < total0 ? i0 : -1;
+      item_s[0] = pre_item;  // slot 0 of the item ring is free at the start
+      mbar_arrive(&itemf_bar[0]);
+      if (pre_item >= 0) {
+        const Item it = decode_item<BN, GATE_UP, MA>(pre_item, n_dense_tiles, b.exp_tiles, tile_off_s, T);
+        const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
+        const int width = min(BN, (it.rows + 15) & ~15);
+        const int na = min(MA, (it.dense ? C::kTilesDense : C::kTilesExp) - it.m * MA);
+        const uint64_t pol_w = (it.nt > 2 && !(it.dense && BN <= 64)) ? policy_evict_last() : policy_evict_first();
+        const CUtensorMap* mp = it.dense ? &map_a_d0 : &map_a_exp;
+        pre_stages = min((nch + C::KC - 1) / C::KC, C::kStages);
+        for (int s2 = 0; s2 < pre_stages; ++s2) {
+          const int c0 = s2 * C::KC, nck = min(C::KC, nch - c0);
+          uint8_t* st = stages + s2 * C::kStageBytes;
+          width_s[s2] = width | (na << 16);
+          mbar_expect_tx(&full_bar[s2], nck * na * kAChunk);
+          for (int cc = 0; cc < nck; ++cc)
+            for (int a = 0; a < na; ++a) {
+              const int tile = it.m * MA + a;
+              tma_load_2d(st + cc * C::kChunkBytes + a * kAChunk, mp, &full_bar[s2], (c0 + cc) * kBK,
+                          it.dense ? tile * kBM : it.e * H + tile * kBM, pol_w);
+            }
+        }
+      }
+    }
+    pre_item = __shfl_sync(0xffffffffu, pre_item, 0);
+    pre_stages = __shfl_sync(0xffffffffu, pre_stages, 0);
+  }
+
   // Everything below reads what earlier kernels of the forward wrote.
   pdl_wait();
   // Dependents may launch now (they run nothing before their own wait that reads this grid's
@@ -313,13 +367,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
   // 613.5 vs 595.7 us). Those launch when the GEMM ends.
   const bool early_dependents = GATE_UP || T <= kEarlyCombineT;
   if (early_dependents) pdl_launch_dependents();
-  const int n_tiles = *reinterpret_cast<volatile int*>(b.n_exp_tiles);
-  const int n_dense_tiles = full_layer ? (T + BN - 1) / BN : 0;
-  // Each role decodes items with a binary search over the experts' first tiles; keep them on chip.
-  __shared__ int tile_off_s[E + 1];
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) tile_off_s[e] = b.tile_off[e];
-  __syncthreads();
-  const int n_dense_items = n_dense_tiles * C::kMtDense;
+  if (!kPreload) load_tiles();
   const int total = n_dense_items + n_tiles * C::kMtExp;
 
   if (warp == 0) {
@@ -334,10 +382,11 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     const uint64_t pol_x = pol_keep;
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t armed = 0, armed_par = 0;  // stages this warp armed, and the parity of the last arm
+    // stages this warp armed, and the parity of the last arm
+    uint32_t armed = (1u << pre_stages) - 1u, armed_par = 0;
     bool ok = true;
     int* sched = b.sched + (GATE_UP ? 0 : 1);
-    int slot = 0;
+    int slot = pre_item != -2 ? 1 : 0;  // the item claimed before the wait took slot 0
     uint32_t slot_par = 0;
     // The next item is claimed one ring's depth of stages before the current one is fully issued:
     // late enough that a CTA busy with a long item does not hold on to work an idle CTA could
@@ -346,19 +395,25 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     bool have_next = false;
     while (ok) {
       int i = -2;
-      if (lane == 0) {
-        if (!have_next) next = atomicAdd(sched, 1);
-        have_next = false;
-        if (mbar_wait_bounded(&iteme_bar[slot], slot_par ^ 1u, abort_flag, b.status, kStatusWaitItem)) {
-          i = next < total ? next : -1;
-          item_s[slot] = i;
-          mbar_arrive(&itemf_bar[slot]);
+      const bool preloaded = pre_item != -2;  // the item claimed (and published) before the wait
+      if (preloaded) {
+        i = pre_item;
+        pre_item = -2;
+      } else {
+        if (lane == 0) {
+          if (!have_next) next = atomicAdd(sched, 1);
+          have_next = false;
+          if (mbar_wait_bounded(&iteme_bar[slot], slot_par ^ 1u, abort_flag, b.status, kStatusWaitItem)) {
+            i = next < total ? next : -1;
+            item_s[slot] = i;
+            mbar_arrive(&itemf_bar[slot]);
+          }
         }
-      }
-      i = __shfl_sync(0xffffffffu, i, 0);
-      if (++slot == kItemSlots) {
-        slot = 0;
-        slot_par ^= 1u;
+        i = __shfl_sync(0xffffffffu, i, 0);
+        if (++slot == kItemSlots) {
+          slot = 0;
+          slot_par ^= 1u;
+        }
       }
       if (i < 0) break;
       const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
@@ -374,7 +429,9 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
       // Converted weights: every A chunk reaches tensor memory through the converter warps, not by TMA.
       const bool a_tma = !CVT;
       for (int c0 = 0; c0 < nch; c0 += C::KC) {
-        if (!warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
+        // A stage armed before the wait holds its weight rows already: only its token rows remain.
+        const bool pre_st = preloaded && c0 / C::KC < pre_stages;
+        if (!pre_st && !warp_wait(&empty_bar[stage], phase ^ 1u, abort_flag, b.status, kStatusWaitEmpty)) {
           ok = false;
           break;
         }
@@ -385,14 +442,18 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
           }
           const int nck = min(C::KC, nch - c0);
           uint8_t* st = stages + stage * C::kStageBytes;
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          width_s[stage] = width | (na << 16);
-          mbar_arrive_expect_tx(&full_bar[stage], nck * ((a_tma ? na * kAChunk : 0) + (b_tma ? C::kBChunk : 0)));
+          if (pre_st) {
+            mbar_arrive_expect_tx(&full_bar[stage], nck * (b_tma ? C::kBChunk : 0));
+          } else {
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            width_s[stage] = width | (na << 16);
+            mbar_arrive_expect_tx(&full_bar[stage], nck * ((a_tma ? na * kAChunk : 0) + (b_tma ? C::kBChunk : 0)));
+          }
           for (int cc = 0; cc < nck; ++cc) {
             uint8_t* a_dst = st + cc * C::kChunkBytes;
             const int k0 = (c0 + cc) * kBK;
-            if (paired) {
+            if (paired && !pre_st) {
               const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
               const CUtensorMap* mu = it.dense ? &map_a_d1 : &map_a_exp;
               const int f0 = it.m * 128;
@@ -403,7 +464,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
               tma_load_2d(a_dst + kAChunk, mu, &full_bar[stage], k0, urow, pol_w);
               tma_load_2d(a_dst + kAChunk + kAChunk / 2, mu, &full_bar[stage], k0, urow + 64, pol_w);
             }
-            for (int a = 0; a < (paired || !a_tma ? 0 : na); ++a) {
+            for (int a = 0; a < (paired || !a_tma || pre_st ? 0 : na); ++a) {
               const int tile = it.m * MA + a;
               if (GATE_UP) {
                 const CUtensorMap* mg = it.dense ? &map_a_d0 : &map_a_exp;
