@@ -153,9 +153,9 @@ constexpr int kKernelsPerForward = 7;
 // is not yet repaid. Layer time, uniform routing, single SMs vs pairs: T = 1500 372.5 vs 384.3 us,
 // 2048 402.9 vs 415.2, 2560 448.1 vs 456.0, 3072 474.8 vs 479.3, 4096 636.0 vs 621.6.
 constexpr int kPairGateUpT = 3072;
-// Batches of at most kRouterFmaT tokens take the router's sums on CUDA cores, with the top-k and
+// Batches of at most kRouteSmallT tokens take the router's sums on CUDA cores, with the top-k and
 // the counting sort in the same kernel (route_small_kernel).
-constexpr int kRouterFmaT = 64;
+constexpr int kRouteSmallT = 64;
 // Largest batch for which the down GEMM lets the combine kernel launch before it ends.
 constexpr int kEarlyCombineT = 64;
 cudaError_t launch_route_small(const RouteParams& p, const Buffers& b, cudaStream_t s);

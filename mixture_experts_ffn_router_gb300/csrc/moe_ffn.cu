@@ -438,7 +438,7 @@ static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weigh
   rp.pre_ff_ln = w->pre_ff_ln;
   rp.pre_ff_ln_2 = w->pre_ff_ln_2;
   rp.T = T;
-  rp.ks = T <= kRouterFmaT ? 1 : choose_ks(T);
+  rp.ks = T <= kRouteSmallT ? 1 : choose_ks(T);
   rp.tpw = choose_tpw(T);
   // Converted experts (int8 or MXFP4) run the GEMM variants with A in tensor memory, built for
   // token tiles of 32 (small batches, deeper rings) or 64.
@@ -533,12 +533,12 @@ static int run_forward(moe_ffn_ctx* c, const void* x, int T, const moe_ffn_weigh
     switch (k) {
       // Small batches: no fold kernel; the router's sums on CUDA cores, the top-k and the counting
       // sort in the same kernel (slot 1), so slots 0, 2 and 3 launch nothing.
-      case 0: e = T <= kRouterFmaT ? cudaSuccess : launch_router_prep(rp, c->buf, s); break;
+      case 0: e = T <= kRouteSmallT ? cudaSuccess : launch_router_prep(rp, c->buf, s); break;
       case 1:
-        e = T <= kRouterFmaT ? launch_route_small(rp, c->buf, s) : launch_router_logits(c->map_wsplit, rp, c->buf, s);
+        e = T <= kRouteSmallT ? launch_route_small(rp, c->buf, s) : launch_router_logits(c->map_wsplit, rp, c->buf, s);
         break;
-      case 2: e = T <= kRouterFmaT ? cudaSuccess : launch_route_topk(rp, c->buf, s); break;
-      case 3: e = T <= kRouterFmaT ? cudaSuccess : launch_route_scatter(rp, c->buf, s); break;
+      case 2: e = T <= kRouteSmallT ? cudaSuccess : launch_route_topk(rp, c->buf, s); break;
+      case 3: e = T <= kRouteSmallT ? cudaSuccess : launch_route_scatter(rp, c->buf, s); break;
       case 4:
         e = cvt     ? launch_gate_up_cvt(bn, f4, gu, c->buf, T, gemm_full, grid_gu, s)
             : pairs_gu ? launch_gate_up_pair(gu, c->buf, pin, T, gemm_full, grid_gu_launch, s)
@@ -676,7 +676,7 @@ static int slots_of(int T, int* slots) {
   if (T == 0) return 0;
   int n = 0;
   for (int k = 0; k < kKernelsPerForward; ++k)
-    if (T > kRouterFmaT || (k != 0 && k != 2 && k != 3)) slots[n++] = k;
+    if (T > kRouteSmallT || (k != 0 && k != 2 && k != 3)) slots[n++] = k;
   return n;
 }
 

@@ -497,7 +497,7 @@ __device__ __forceinline__ void write_norm_row(const RouteParams& p, const Buffe
 }
 
 // ------------------------------------------------------------------------------------------
-// Small batches (T <= kRouterFmaT): the routing front end in one kernel, three phases chained by
+// Small batches (T <= kRouteSmallT): the routing front end in one kernel, three phases chained by
 // tickets rather than by kernel boundaries.
 //   1. CTA (x, g) forms W'[e] = W_r[e] * (1 + router_norm_w) in fp32 for the four experts
 //      e = 4x .. 4x + 3 and the raw router sums of tokens 16g .. 16g + 15, two per warp, both rows
@@ -516,7 +516,7 @@ __device__ __forceinline__ void write_norm_row(const RouteParams& p, const Buffe
 constexpr int kSmallTok = 16;  // tokens per CTA: two per warp
 constexpr int kSmallExp = 4;   // experts per CTA
 constexpr int kSmallFinal = 4; // small_ctr index of the phase-3 ticket (0..3: token groups)
-static_assert(kRouterFmaT <= 64 && kRouterFmaT <= 4 * kSmallTok, "token masks and group tickets");
+static_assert(kRouteSmallT <= 64 && kRouteSmallT <= 4 * kSmallTok, "token masks and group tickets");
 static_assert(E / kSmallExp == 2 * kSmallTok, "one row job (n1 or n2 of a token) per CTA of a group");
 
 __global__ void __launch_bounds__(256) route_small_kernel(RouteParams p, Buffers b) {
@@ -957,7 +957,7 @@ cudaError_t launch_route_topk(const RouteParams& p, const Buffers& b, cudaStream
 }
 
 cudaError_t launch_route_small(const RouteParams& p, const Buffers& b, cudaStream_t s) {
-  if (p.T < 1 || p.T > kRouterFmaT) return cudaErrorInvalidValue;
+  if (p.T < 1 || p.T > kRouteSmallT) return cudaErrorInvalidValue;
   return launch_pdl(route_small_kernel, dim3(E / kSmallExp, (p.T + kSmallTok - 1) / kSmallTok), dim3(256), 0, s, p, b);
 }
 

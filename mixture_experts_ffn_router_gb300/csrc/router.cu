@@ -15,6 +15,8 @@
 //     64-wide chunk of h is summed on the tensor cores (3 parts x 64 products) into its own TMEM
 //     accumulator, and the chunk sums are added in fp32 registers, so the tensor core's own
 //     accumulation spans only the 192 products of one chunk.
+// Batches of more than kRouteSmallT tokens use these two kernels; smaller ones take the same sums in
+// fp32 on CUDA cores inside the small-batch routing kernel (route.cu), with no fold kernel.
 // MMA: M = 128 experts (A = a W' part, K-major, by TMA), N = 128 tokens (B = x rows, K-major,
 // staged by the producer warp). Warp 0 loads, warp 1 issues the MMAs, warps 2..9 add chunk sums
 // (two per TMEM lane quarter, half of the token columns each).
