@@ -393,12 +393,19 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
     // take, early enough that the atomic's round trip overlaps the loads still to come.
     int next = 0;
     bool have_next = false;
+    // Converted weights: the weight-row producer's ring holds 20 (int8) or 40 (MXFP4) K chunks, far
+    // more than this warp's stage ring runs ahead of the MMAs, so each item is claimed and published
+    // when the one before it starts (-3: none published ahead).
+    int pub_next = -3;
     while (ok) {
       int i = -2;
       const bool preloaded = pre_item != -2;  // the item claimed (and published) before the wait
       if (preloaded) {
         i = pre_item;
         pre_item = -2;
+      } else if (pub_next != -3) {
+        i = pub_next;
+        pub_next = -3;
       } else {
         if (lane == 0) {
           if (!have_next) next = atomicAdd(sched, 1);
@@ -416,6 +423,24 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
         }
       }
       if (i < 0) break;
+      if (CVT) {
+        int n2 = -2;
+        if (lane == 0) {
+          const int nx = atomicAdd(sched, 1);
+          if (mbar_wait_bounded(&iteme_bar[slot], slot_par ^ 1u, abort_flag, b.status, kStatusWaitItem)) {
+            n2 = nx < total ? nx : -1;
+            item_s[slot] = n2;
+            mbar_arrive(&itemf_bar[slot]);
+          }
+        }
+        n2 = __shfl_sync(0xffffffffu, n2, 0);
+        if (++slot == kItemSlots) {
+          slot = 0;
+          slot_par ^= 1u;
+        }
+        if (n2 == -2) break;  // gave up waiting (the status word says why)
+        pub_next = n2;
+      }
       const Item it = decode_item<BN, GATE_UP, MA>(i, n_dense_tiles, b.exp_tiles, tile_off_s, T);
       const int nch = it.dense ? C::kChunksDense : C::kChunksExp;
       const bool b_tma = !GATE_UP || it.dense;
@@ -436,7 +461,7 @@ __global__ void __launch_bounds__(Cfg<BN, GATE_UP, MA, QW>::kThreads, 1)
           break;
         }
         if (lane == 0) {
-          if (!have_next && c0 + C::kStages * C::KC >= nch) {
+          if (!CVT && !have_next && c0 + C::kStages * C::KC >= nch) {
             next = atomicAdd(sched, 1);
             have_next = true;
           }
