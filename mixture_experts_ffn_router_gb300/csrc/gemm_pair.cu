@@ -21,7 +21,10 @@
 // gate and up of a feature land in the same TMEM lane, so the epilogue forms gelu_tanh(g) * u with
 // no hand-over. The two accumulators fill TMEM (2 x 256 columns), so they are single-buffered and
 // drained by eight epilogue warps. down keeps one tile per CTA (its K = 704 is too short to hide a
-// single-buffered epilogue) and double-buffers its accumulator.
+// single-buffered epilogue) and double-buffers its accumulator; even so, one item's 11 K chunks
+// take about as long as draining the accumulator with one warp per TMEM lane quarter, so down also
+// drains with eight warps, two per quarter taking half the token columns each (T = 4096: 181 vs
+// 198 us; sixteen warps: 189 us).
 //
 // Layout of one work item (a token tile of up to 256 slots and the pair's weight rows):
 //   * gate_up: rank r holds features f = 256 m + 128 r .. + 127 (gate rows in tile 0, up rows in
@@ -65,7 +68,7 @@ struct PCfg {
   static constexpr int kStage = MA * kPAChunk + kPBChunk;                // 48 | 32 KB
   static constexpr int kStages = GATE_UP ? 4 : 6;
   static constexpr int kNAcc = GATE_UP ? 1 : 2;                          // accumulator sets (buffers)
-  static constexpr int kEpiWarps = GATE_UP ? 8 : 4;
+  static constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, half the token columns each
   static constexpr int kThreads = (2 + kEpiWarps) * 32;                  // producer, MMA, epilogue
   // Item-slot consumers, all counted on the leader's release barrier: the leader's MMA thread and
   // epilogue warps, the peer's producer and epilogue warps.
@@ -75,7 +78,7 @@ struct PCfg {
   static constexpr int kMtDense = GATE_UP ? (D + kFeat - 1) / kFeat : H / (2 * kPRows);  // 9 | 11
   static constexpr int kChunksExp = GATE_UP ? H / kPBK : I / kPBK;      // 44 | 11 K chunks
   static constexpr int kChunksDense = GATE_UP ? H / kPBK : D / kPBK;    // 44 | 33
-  static constexpr int kXchgBytes = kEpiWarps * (GATE_UP ? 32 * 32 * 2 : 32 * 32 * 4);  // staging
+  static constexpr int kXchgBytes = kEpiWarps * 32 * 32 * 2;  // staging: 32 x 32 bf16 per warp
   static constexpr int kBarBytes = 512;
   static constexpr int kBarNeed = 8 * (2 * kStages + 2 * kNAcc + 1 + 2 * kPItemSlots) + 8 + 4 * kPItemSlots;
   static constexpr int kSmem = 1024 + kStages * kStage + kXchgBytes + kBarBytes;
@@ -430,9 +433,10 @@ __global__ void __launch_bounds__(PCfg<GATE_UP>::kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue warps (both CTAs): TMEM lane quarter q = warp % 4. gate_up: the two
-    // warps of a quarter take half of the token columns each; down: one warp per quarter.
+    // warps of a quarter take half of the token columns each (down likewise).
     const int q = warp & 3;
-    const int chalf = GATE_UP ? (warp - 2) >> 2 : 0;
+    const int chalf = (warp - 2) >> 2;             // which share of the token columns
+    constexpr int kColChunks = kPBN / 32 / (C::kEpiWarps / 4);  // 32-column chunks per warp
     if (GATE_UP) {
       // First, before any accumulator is ready: the experts' input in sorted-slot order. Warp w of
       // the grid takes tokens w, w + warps, ...: n2 = x / RMS(x) * (1 + pre_feedforward_layernorm_2)
@@ -562,9 +566,9 @@ __global__ void __launch_bounds__(PCfg<GATE_UP>::kThreads, 1)
         }
       } else {
         const int f0 = (it.m * 2 + static_cast<int>(rank)) * kPRows + 32 * q;
-        uint8_t* stg = xchg + q * 4096;
+        uint8_t* stg = xchg + (warp - 2) * 2048;
 #pragma unroll 1
-        for (int c = 0; c < kPBN / 32; ++c) {
+        for (int c = chalf * kColChunks; c < (chalf + 1) * kColChunks; ++c) {
           if (c * 32 >= it.rows) break;
           float v[32];
           tmem_ld32(t_row + c * 32, v);
