@@ -702,21 +702,34 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteParams p, Buffers
 __global__ void __launch_bounds__(256) route_scatter_kernel(RouteParams p, Buffers b) {
   __shared__ uint32_t mask_s[8][E];
   __shared__ int pre_s[8][E];
+  __shared__ int base_s[E];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 8 * E; i += 256) (&mask_s[0][0])[i] = 0u;
   pdl_wait();
   pdl_launch_dependents();
-  __syncthreads();
-  const int t = blockIdx.x * kScatterTok + warp * 32 + lane;
+  const int b0 = blockIdx.x;
+  const int t = b0 * kScatterTok + warp * 32 + lane;
   const bool valid = t < p.T;
-  int ids[K];
+  // Every load this CTA needs is issued here, so that it waits for memory once: the token's expert
+  // ids and weights (16-byte vectors) and the CTA's base positions.
+  int4 ia = make_int4(0, 0, 0, 0), ib = ia;
+  float4 wa = make_float4(0.0f, 0.0f, 0.0f, 0.0f), wb = wa;
+  if (valid) {
+    ia = *reinterpret_cast<const int4*>(b.topk_idx + static_cast<size_t>(t) * K);
+    ib = *reinterpret_cast<const int4*>(b.topk_idx + static_cast<size_t>(t) * K + 4);
+    wa = *reinterpret_cast<const float4*>(b.topk_w + static_cast<size_t>(t) * K);
+    wb = *reinterpret_cast<const float4*>(b.topk_w + static_cast<size_t>(t) * K + 4);
+  }
+  if (tid < E) base_s[tid] = b.base[b0 * E + tid];
+  __syncthreads();
+  int ids[K] = {ia.x, ia.y, ia.z, ia.w, ib.x, ib.y, ib.z, ib.w};
+  const float ws[K] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
   for (int k = 0; k < K; ++k) {
-    ids[k] = valid ? b.topk_idx[static_cast<size_t>(t) * K + k] : 0;
     if (valid) {
       if (ids[k] < 0 || ids[k] >= E) {
         atomicOr(b.status, kStatusBadIndex);
-        ids[k] = 0;
+        ids[k] = -1;
       } else {
         atomicOr(&mask_s[warp][ids[k]], 1u << lane);
       }
@@ -733,19 +746,19 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteParams p, Buffe
   }
   __syncthreads();
   if (!valid) return;
-  const int b0 = blockIdx.x;
   const uint32_t lt = (1u << lane) - 1u;
   const int S = p.T * K;
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int e = ids[k];
-    const int pos = b.base[b0 * E + e] + pre_s[warp][e] + __popc(mask_s[warp][e] & lt);
+    if (e < 0) continue;
+    const int pos = base_s[e] + pre_s[warp][e] + __popc(mask_s[warp][e] & lt);
     if (pos < 0 || pos >= S) {
       atomicOr(b.status, kStatusBadIndex);
       continue;
     }
     b.perm[pos] = t;
-    b.w_sorted[pos] = b.topk_w[static_cast<size_t>(t) * K + k];
+    b.w_sorted[pos] = ws[k];
     b.slot_pos[static_cast<size_t>(t) * K + k] = pos;
   }
 }
