@@ -49,6 +49,13 @@ def test_full_layer(T):
     _full_check(FULL, T, 200 + T, label="full T=%d" % T)
 
 
+@pytest.mark.parametrize("T", [65, 300])
+def test_moe_only_above_small_batches(T):
+    # The experts-only block above 64 tokens: the router, top-k and scatter kernels run apart, and
+    # the combine sums each token's 8 rows of y with no norms.
+    _full_check(MOE, T, 150 + T, label="moe-only T=%d" % T)
+
+
 def test_kernel_slots_by_batch_size():
     m = B.MoeFFN(FULL, 256)
     for T in (1, 17, 64):
