@@ -60,7 +60,7 @@ extern "C" {
 #define MOE_FFN_STATUS_DRAIN 0x40u          /* an exit drain gave up waiting for work in flight */
 #define MOE_FFN_STATUS_WAIT_ITEM 0x80u      /* a GEMM role gave up waiting for its next work item */
 #define MOE_FFN_STATUS_WAIT_COPY 0x100u     /* a GEMM producer gave up waiting for the sorted copy of
-                                               its token rows (forwards above 1024 tokens) */
+                                               its token rows (forwards above 3072 tokens) */
 
 /* Modes. */
 #define MOE_FFN_MOE_ONLY 0    /* router + experts only: out = sum of the 8 weighted expert outputs */
@@ -145,7 +145,7 @@ typedef struct moe_ffn_views {
   const int32_t* slot_pos;    /* [T, 8] sorted position of slot (t, k) */
   const uint16_t* n1;         /* [T, 2816] bf16 pre_feedforward_layernorm(x) (FULL_LAYER) */
   const uint16_t* n2;         /* [T, 2816] bf16 expert input: pre_feedforward_layernorm_2(x), or x
-                               (forwards of at most 1024 tokens or with converted experts; larger
+                               (forwards of at most 3072 tokens or with converted experts; larger
                                ones write it in sorted-slot order into the y buffer instead, which the
                                down GEMM then overwrites) */
   const uint16_t* h;          /* [S, 704] bf16 gelu_tanh(gate) * up per sorted slot */
